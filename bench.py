@@ -1,0 +1,449 @@
+"""Benchmark: one mixed chunked-prefill + decode step (paged KV append + fused
+attention forward + split combine) on synthetic inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+Prints ONE JSON line (rank 0).  ``value`` is query tokens per second over the
+timed steps (all ranks), ``ms_per_step`` the device time of one step.  The
+default workload is the worked A/B/C layout (cu_seqlens_q = [0, 1, 2, 1810],
+seqlens_k = [121, 46, 10000], 32 q / 8 kv heads, head_dim 128, 16-token pages).
+``--impl reference`` times the CPU oracle on a bounded sample instead.
+Under torchrun every rank runs an independent replica (the step does not
+shard); timing is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "mixed prefill+decode paged-attn step µs, tokens/s, % of HBM/TC roofline"
+UNIT = "query tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work of one step (what the method must move / compute)
+# ---------------------------------------------------------------------------
+
+def algorithmic(w):
+    """Bytes and tensor FLOPs of one step, per the roofline definition: every
+    KV position read once per kv head (K and V), Q read and O written once;
+    the append reads and writes the new rows; tensor FLOPs are the visible
+    (query, key) pairs of the chunk segments x 2 matmuls x 2 flops x D x H_q."""
+    D, Hq, Hkv = w.head_dim, w.num_q_heads, w.num_kv_heads
+    kv_bytes = sum(w.k_lens[s] for s in range(w.num_seqs) if w.q_lens[s] > 0) * Hkv * D * 2 * 2
+    q_bytes = w.total_q * Hq * D * 2
+    o_bytes = w.total_q * Hq * D * 2
+    append_bytes = w.total_q * Hkv * D * 2 * 2 * 2
+    G = Hq // Hkv
+    flops_tc = 0
+    flops_dec = 0
+    for lq, lk in zip(w.q_lens, w.k_lens):
+        pairs = lq * (lk - lq) + lq * (lq + 1) // 2
+        if lq * G > 16:
+            flops_tc += 4 * D * Hq * pairs
+        else:
+            flops_dec += 4 * D * Hq * pairs
+    return dict(kv_bytes=kv_bytes, q_bytes=q_bytes, o_bytes=o_bytes, append_bytes=append_bytes,
+                fwd_bytes=kv_bytes + q_bytes + o_bytes, flops_tc=flops_tc, flops_dec=flops_dec)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return dict(hbm=float(m["hbm_gbs"]), bf16=float(m["bf16_tflops"]),
+                    bf16_sustained=float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("attn_fwd.cu", "ptx.cuh", "mcp_internal.h"):
+        with open(os.path.join(ROOT, "mixed_chunked_prefill_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the fused kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"mixed_attn_fwd_kernel.{workload}.md")
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_sha():
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.devnull if False else "/tmp/_mcp_clocks_%d.csv" % os.getpid(), "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import mixed_chunked_prefill_gb300 as mcp
+    from mixed_chunked_prefill_gb300 import build as mcp_build
+    from mixed_chunked_prefill_gb300.step import HostStep, MixedStep, write_history
+
+    if rank == 0 or not os.path.exists(mcp_build.LIB_PATH):
+        mcp_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    mcp.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    w = synth.make_workload(args.config)
+    alg = algorithmic(w)
+    peaks = load_peaks()
+
+    with torch.cuda.stream(stream):
+        t = w.tensors(dev)
+        shape = (w.num_pages, w.page_size, w.num_kv_heads, w.head_dim)
+        k_cache = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        v_cache = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        bt = w.block_tables()
+        write_history(bt, w.hist_lens, t["k_hist"], t["v_hist"], k_cache, v_cache, w.page_size,
+                      stream=stream)
+        del t["k_hist"], t["v_hist"]
+        cu = np.concatenate([[0], np.cumsum(w.q_lens)]).astype(np.int32)
+        t0 = time.perf_counter()
+        step = MixedStep(w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size, w.num_pages,
+                         w.sm_scale, cu, w.k_lens, bt, device=dev, stream=stream)
+        plan_us = (time.perf_counter() - t0) * 1e6
+        q, k_new, v_new = t["q"], t["k_new"], t["v_new"]
+        out = torch.empty_like(q)
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream.synchronize()
+
+    def one_step():
+        step.run(q, k_new, v_new, k_cache, v_cache, out)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            one_step()
+    step.check()
+
+    # timed region: K steps, L2 flushed (untimed) between steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    fwd_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            step.append(k_new, v_new, k_cache, v_cache)
+            fwd_evs[i][0].record(stream)
+            step.attention(q, k_cache, v_cache, out)
+            fwd_evs[i][1].record(stream)
+            evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    step.check()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    fwd_ms = [a.elapsed_time(b) for a, b in fwd_evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    tokens_per_s = world * w.total_q * args.steps / (total_ms / 1e3)
+
+    # end to end through the C ABI from pinned host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        q_h = q.cpu().pin_memory()
+        k_h = k_new.cpu().pin_memory()
+        v_h = v_new.cpu().pin_memory()
+        out_h = torch.empty_like(q_h).pin_memory()
+        hs = HostStep(w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size, w.num_pages,
+                      w.sm_scale, w.total_q, w.num_seqs, w.max_pages_per_seq, device=dev,
+                      stream=stream)
+        for _ in range(3):
+            hs(q_h, k_h, v_h, cu, w.k_lens, bt, k_cache, v_cache, out_h)
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            hs(q_h, k_h, v_h, cu, w.k_lens, bt, k_cache, v_cache, out_h)
+        stream.synchronize()
+        e2e_s = time.perf_counter() - t0
+        if world > 1:
+            tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e2e_s = float(tt.item())
+        e2e = {"value": world * w.total_q * args.e2e_steps / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": int(hs.h2d_bytes), "d2h_bytes_per_step": int(hs.d2h_bytes),
+               "ms_per_step": 1e3 * e2e_s / args.e2e_steps, "steps": args.e2e_steps}
+
+    # roofline of the dominant kernel (the fused forward; its call also runs
+    # the split combine when the plan has splits)
+    fwd_avg_s = statistics.mean(fwd_ms) / 1e3
+    t_tc = alg["flops_tc"] / (peaks["bf16"] * 1e12)
+    t_hbm = alg["fwd_bytes"] / (peaks["hbm"] * 1e9)
+    if t_tc >= t_hbm:
+        achieved = alg["flops_tc"] / fwd_avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16"]}
+    else:
+        achieved = alg["fwd_bytes"] / fwd_avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm"]}
+    roof["traffic"] = profiled_traffic(args.config)
+    roof["peak_source"] = f"{peaks['source']} ({'burst bf16' if roof['bound'] == 'tensor' else 'copy'})"
+    roof["kernel_ms"] = statistics.mean(fwd_ms)
+    step_roof_s = max(t_tc, (alg["fwd_bytes"] + alg["append_bytes"]) / (peaks["hbm"] * 1e9))
+    launches_per_step = 2 + (1 if step.plan.num_combine > 0 else 0)
+    res = {
+        "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
+        "config": {"workload": synth.DESCRIPTIONS[args.config], "name": args.config,
+                   "segments": w.num_seqs, "total_q": w.total_q,
+                   "kv_tokens": int(sum(w.k_lens)), "l2": "flushed between steps (256 MB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "step": "paged_kv_append + mixed_attn_fwd (+ combine)",
+                   "work_items": int(step.plan.num_items),
+                   "decode_items": int(step.plan.num_decode_items),
+                   "prefill_items": int(step.plan.num_prefill_items),
+                   "combine_groups": int(step.plan.num_combine)},
+        "step_us": ms_per_step * 1e3,
+        "step_us_p10_p90": [float(np.percentile(step_ms, 10) * 1e3),
+                            float(np.percentile(step_ms, 90) * 1e3)],
+        "kv_gbps": alg["kv_bytes"] / (ms_per_step / 1e3) / 1e9,
+        "step_roofline_frac": step_roof_s / (ms_per_step / 1e3),
+        "plan_host_us": plan_us,
+        "roofline": roof,
+        "clocks": clk,
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e,
+    }
+    return res
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_cores():
+    try:
+        import threadpoolctl
+
+        info = threadpoolctl.threadpool_info()
+        n = max((i.get("num_threads", 1) for i in info), default=1)
+        return int(n)
+    except Exception:
+        return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+class OracleSample:
+    """The oracle on one workload's inputs, restricted to a row sample."""
+
+    def __init__(self, name):
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        import torch
+
+        from harness import OracleStep
+
+        w = synth.make_workload(name)
+        self.w = w
+        if name in ("decode-heavy", "long-context"):
+            # too large to hold whole: keep the chunk and two decodes
+            from gpu_harness import sub_workload
+
+            t = w.tensors("cpu")
+            dec = [s for s in range(w.num_seqs) if w.q_lens[s] == 1][:2]
+            chunk = [s for s in range(w.num_seqs) if w.q_lens[s] > 1]
+            w, t = sub_workload(w, t, dec + chunk)
+            self.w = w
+            self.note = "two decodes + the chunk segment of the workload"
+        else:
+            t = w.tensors("cpu")
+            self.note = "all segments"
+        self.step = OracleStep(w, t)
+        self.step.do_append()
+        del torch
+
+    def rows(self, n):
+        """n query tokens spread over the whole stream (decodes first)."""
+        T = self.w.total_q
+        n = max(1, min(n, T))
+        return sorted(set(np.linspace(0, T - 1, n).round().astype(int).tolist()))
+
+    def time_rows(self, rows):
+        t0 = time.perf_counter()
+        self.step.attention(tokens=rows)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(name, budget_s=15.0):
+    s = OracleSample(name)
+    rows = s.rows(4)
+    dt = s.time_rows(rows)
+    n = len(rows)
+    # the per-segment K/V gather is a fixed cost, so grow the row sample until
+    # the timed call reaches about half the budget (or covers every row)
+    while dt < budget_s / 2 and n < s.w.total_q:
+        n = min(s.w.total_q, n * 4)
+        rows = s.rows(n)
+        dt = s.time_rows(rows)
+    return {"value": len(rows) / dt, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",
+            "sample": f"{len(rows)} of {s.w.total_q} query tokens (all heads), {s.note}; "
+                      f"{dt:.1f} s", "seconds": dt}
+
+
+def run_reference(args):
+    s = OracleSample(args.config)
+    budget = 150.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    rows = s.rows(2)
+    dt = s.time_rows(rows)
+    n = len(rows)
+    while dt < per_step / 4 and n < s.w.total_q:
+        n = min(s.w.total_q, n * 2)
+        rows = s.rows(n)
+        dt = s.time_rows(rows)
+    for _ in range(args.warmup):
+        s.time_rows(rows)
+    times = [s.time_rows(rows) for _ in range(args.steps)]
+    total = sum(times)
+    value = len(rows) * args.steps / total
+    sample = (f"{len(rows)} of {s.w.total_q} query tokens (all heads) per step, {s.note}")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
+            "config": {"workload": synth.DESCRIPTIONS[args.config], "name": args.config},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="worked", choices=synth.CONFIG_NAMES)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = cpu_baseline(args.config)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

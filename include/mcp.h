@@ -1,0 +1,277 @@
+/*
+ * mcp.h -- C ABI of the mixed chunked-prefill + decode paged-attention library
+ * (GB300, sm_103a).
+ *
+ * One step of a chunked-prefill serving engine packs decode segments (one
+ * query token each) and prefill chunks (many query tokens) into one token
+ * stream.  For every layer the step (1) writes each new token's K/V into its
+ * physical page through a slot mapping, then (2) runs one fused attention
+ * forward over the whole stream, each segment against its own paged KV with the
+ * query segment right-aligned to the end of its KV segment.
+ *
+ * Pages this follows (title, section):
+ *   [W] wangyu.me, "大语言模型推理优化（二）：Chunked Prefill" -- sections
+ *       "组装长序列", "记录 KV Cache 的长度", "Flash Attention 的 varlen 接口",
+ *       "输入组装".
+ *   [L] lpnh.cn, "技术融合剖析：Chunked Prefill如何借助FlashAttention/FlashInfer
+ *       实现混合批次推理" -- sections 3.1 (packed Q/K/V and cu_seqlens),
+ *       4.1 (block tables), 4.2 (append_paged_kv_cache).
+ *   [K] kwkr.cn, hybrid-batch Chunked Prefill page -- sections
+ *       "混合批次计算图与内存访问不对称性" (paged KV scattered in HBM),
+ *       "平铺策略 / 掩码特化" (one fused kernel, mask only on the chunk's
+ *       diagonal), "Triton 混合算子内核设计与实现" (online softmax).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every tensor is caller-owned.  Device tensors are dense, row-major,
+ *    16-byte aligned; bf16 is IEEE bfloat16 stored as 2 bytes.
+ *  - The library allocates no device memory.  Calls that need scratch take a
+ *    caller-provided device workspace sized by mcp_mixed_attn_plan().
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Device work is enqueued asynchronously on it; host-only calls ignore it.
+ *  - Return value: MCP_OK, or an mcp_status error.  Argument errors are found on
+ *    the host before anything is launched; nothing is written in that case.
+ *    mcp_last_error() gives a one-line description of the last failure on the
+ *    calling thread.  No C++ exception crosses this boundary.
+ *  - Layouts (shapes are [outer, ..., inner]):
+ *      q, out        [T, H_q, D]        bf16   T = cu_seqlens_q[S]
+ *      k_new, v_new  [T, H_kv, D]       bf16
+ *      k/v cache     [num_pages, P, H_kv, D] bf16 ("NHD" pages, K and V apart)
+ *      block_tables  [S, max_pages_per_seq] int32, logical -> physical page
+ *      cu_seqlens_q  [S + 1] int32, exclusive prefix sum of query lengths
+ *      seqlens_k     [S] int32, KV length of each segment INCLUDING this
+ *                    step's tokens ([W] "记录 KV Cache 的长度")
+ *      slot_mapping  [T] int64, physical_page * P + offset; < 0 = skip
+ *      lse           [T, H_q] float32, natural-log sum of exp of the scores
+ *    Query head h uses kv head h / (H_q / H_kv) (grouped-query attention;
+ *    with H_q == H_kv this is [K]'s multi-head indexing).
+ */
+#ifndef MCP_H_
+#define MCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MCP_ABI_VERSION 1
+
+typedef enum mcp_status {
+  MCP_OK = 0,
+  MCP_ERR_INVALID_ARG = 1,         /* bad pointer, size, layout or metadata        */
+  MCP_ERR_UNSUPPORTED = 2,         /* valid but not built (e.g. head_dim 96)       */
+  MCP_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace smaller than the plan needs        */
+  MCP_ERR_CUDA = 4,                /* a CUDA runtime/driver call failed            */
+  MCP_ERR_TIMEOUT = 5,             /* a device-side bounded wait gave up           */
+  MCP_ERR_DEVICE_CHECK = 6         /* a device-side range check failed             */
+} mcp_status;
+
+/* Static string for a status code (never NULL). */
+const char* mcp_status_string(int32_t status);
+
+/* One-line description of the last non-OK return on this thread ("" if none). */
+const char* mcp_last_error(void);
+
+/* MCP_ABI_VERSION of the loaded library. */
+int32_t mcp_abi_version(void);
+
+/* ------------------------------------------------------------------------- */
+/* a1: paged KV append                                                       */
+/* ------------------------------------------------------------------------- */
+/*
+ * Copy each new token's K and V rows into its physical slot of the paged
+ * caches: for t in [0, num_tokens) with s = slot_mapping[t] >= 0,
+ *   k_cache[s / P][s % P][:][:] = k_new[t][:][:]   (and the same for v).
+ * Tokens with s < 0 are padding and are skipped.  This is the "write new K/V
+ * through slot_mapping, then run attention" step of [W] "输入组装" and [L] 4.2
+ * (physical address translation, scattered writes).  Slots must be distinct
+ * within one call (the result is then independent of thread order; [L] 4.2's
+ * atomics are not needed).  Slots >= num_pages * P are not written and are
+ * reported by mcp_check_device_errors() as MCP_ERR_DEVICE_CHECK.
+ *
+ * k_new, v_new  device, bf16 [num_tokens, num_kv_heads, head_dim]
+ * slot_mapping  device, int64 [num_tokens]
+ * k_cache, v_cache device, bf16 [num_pages, page_size, num_kv_heads, head_dim]
+ * error_word    device int32, or NULL; receives device-check bits (see below)
+ * Requirements: num_tokens >= 0; (num_kv_heads * head_dim) % 8 == 0.
+ * Bit-exact: the bytes of the new rows are copied unchanged.
+ */
+mcp_status mcp_paged_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                               int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t page_size, int32_t num_pages, void* k_cache, void* v_cache,
+                               int32_t* error_word, void* stream);
+
+/*
+ * Host helper for step assembly: the slot of every new token of the step
+ * ([W] "输入组装").  Segment s's tokens are its last Lq_s KV positions,
+ * Lq_s = cu_seqlens_q[s+1] - cu_seqlens_q[s], so token t of segment s sits at
+ * position pos = seqlens_k[s] - Lq_s + (t - cu_seqlens_q[s]) and gets
+ *   slot = block_tables[s][pos / P] * P + pos % P.
+ * All pointers are HOST memory.  slot_mapping receives cu_seqlens_q[S] values.
+ * Returns MCP_ERR_INVALID_ARG on malformed metadata or a page id outside
+ * [0, num_pages).
+ */
+mcp_status mcp_build_slot_mapping(const int32_t* block_tables, int32_t num_seqs,
+                                  int32_t max_pages_per_seq, int32_t page_size, int32_t num_pages,
+                                  const int32_t* cu_seqlens_q, const int32_t* seqlens_k,
+                                  int64_t* slot_mapping);
+
+/* ------------------------------------------------------------------------- */
+/* a2..a9: mixed attention forward                                           */
+/* ------------------------------------------------------------------------- */
+
+typedef struct mcp_attn_desc {
+  int32_t num_seqs;          /* S, segments in the stream                        */
+  int32_t total_q;           /* T = cu_seqlens_q[S]                              */
+  int32_t num_q_heads;       /* H_q                                              */
+  int32_t num_kv_heads;      /* H_kv; must divide H_q                            */
+  int32_t head_dim;          /* D: 64 or 128                                     */
+  int32_t page_size;         /* P: 16                                            */
+  int32_t max_pages_per_seq; /* row length of block_tables                       */
+  int32_t num_pages;         /* pages in each cache tensor                       */
+  float sm_scale;            /* score scale, e.g. 1/sqrt(D) ([K] kernel launch)  */
+} mcp_attn_desc;
+
+typedef struct mcp_plan_options {
+  int32_t num_sms;              /* 0 = query the current device                  */
+  int32_t decode_split_tokens;  /* KV tokens per decode work item; 0 = auto      */
+  int32_t prefill_split_tokens; /* KV tokens per prefill work item; 0 = auto     */
+  int32_t reserved[5];          /* must be 0                                     */
+} mcp_plan_options;
+
+/* Filled by mcp_mixed_attn_plan(); read by mcp_mixed_attn_fwd().  Plain data:
+ * it may be copied; its fields describe the workspace layout. */
+typedef struct mcp_plan {
+  int32_t magic;
+  int32_t num_items;          /* work items (CTAs of the fused kernel)           */
+  int32_t num_decode_items;   /* items on the decode (split-KV) path             */
+  int32_t num_prefill_items;  /* items on the tensor-core chunk path             */
+  int32_t num_combine;        /* row groups merged by the combine kernel         */
+  int32_t decode_split_tokens;
+  int32_t prefill_split_tokens;
+  int32_t num_sms;
+  int64_t partial_rows;       /* rows of split partial results                   */
+  int64_t off_items, off_combine, off_part_o, off_part_lse, off_error;
+  int64_t workspace_bytes;    /* bytes the workspace must have                   */
+  mcp_attn_desc desc;         /* the description the plan was built for          */
+  int32_t reserved[8];
+} mcp_plan;
+
+/*
+ * Plan one step.  Validates the step's metadata on the host and splits it
+ * into work items for the fused kernel:
+ *  - a segment with Lq * G <= 16 (G = H_q / H_kv) goes to the decode path:
+ *    one item per (kv head, KV range); its G*Lq query rows share each K/V page;
+ *  - any other segment goes to the tensor-core path: one item per (kv head,
+ *    tile of 128/G query tokens, KV range), the G query heads of a kv head
+ *    packed into 128 rows.
+ * Long KV ranges are split; the combine kernel merges the splits.  Items are
+ * ordered so the longest go first and tiles reading the same K/V run side by
+ * side.
+ *
+ * h_cu_seqlens_q [S+1], h_seqlens_k [S]: HOST copies of the step metadata.
+ * opts: may be NULL (all defaults).
+ * Requirements ([W] "Flash Attention 的 varlen 接口"): cu_seqlens_q[0] == 0,
+ * non-decreasing, cu_seqlens_q[S] == total_q; 0 <= Lq_s <= seqlens_k[s],
+ * seqlens_k[s] >= 1 when Lq_s > 0; ceil(seqlens_k[s] / P) <= max_pages_per_seq.
+ *
+ * workspace == NULL: sizing only; *plan receives the work counts and
+ *   plan->workspace_bytes; nothing is copied and `stream` is unused.
+ * workspace != NULL: device memory of workspace_bytes >= plan->workspace_bytes,
+ *   256-byte aligned.  The work lists are copied into it on `stream` (from a
+ *   host buffer that is staged before this call returns) and its device error
+ *   word is cleared.  A workspace must not be re-planned while a previous
+ *   mcp_mixed_attn_fwd that uses it is still running on another stream.
+ */
+mcp_status mcp_mixed_attn_plan(const mcp_attn_desc* desc, const int32_t* h_cu_seqlens_q,
+                               const int32_t* h_seqlens_k, const mcp_plan_options* opts,
+                               mcp_plan* plan, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
+ * Same plan as mcp_mixed_attn_plan, written to HOST memory instead of a
+ * device workspace: host_buffer receives the first plan->off_part_o bytes of
+ * the workspace layout (the work items at plan->off_items and the combine
+ * entries at plan->off_combine).  A caller that copies those bytes to the
+ * start of its device workspace and zeroes the 4-byte error word at
+ * plan->off_error gets the same state mcp_mixed_attn_plan uploads.
+ * host_buffer == NULL: sizing only.  Host only; needs no GPU when
+ * opts->num_sms > 0.  Item layout (32 bytes, int32 fields): segment, kv head,
+ * kind (0 decode, 1 tensor-core tile), first query token inside the segment,
+ * query token count, first key, one past the last key, partial row (-1 =
+ * written directly).  Combine entry (32 bytes, int32): segment, kv head, first
+ * query token, query token count, number of splits, first partial row, rows
+ * per split, 0.
+ */
+mcp_status mcp_mixed_attn_plan_host(const mcp_attn_desc* desc, const int32_t* h_cu_seqlens_q,
+                                    const int32_t* h_seqlens_k, const mcp_plan_options* opts,
+                                    mcp_plan* plan, void* host_buffer, size_t host_bytes);
+
+/*
+ * The fused mixed attention forward ([W] "Flash Attention 的 varlen 接口":
+ * the i-th query segment attends only to the i-th KV segment, right-aligned
+ * causal; [K] "平铺策略 / 掩码特化": one kernel for prefill chunks and
+ * decodes).  For every segment s, query head h and query i in [0, Lq_s):
+ *   s_j  = sm_scale * <q[i,h], k_j>  for KV positions j <= i + (Lk_s - Lq_s)
+ *   out[i,h] = sum_j softmax(s)_j v_j,   lse[i,h] = ln sum_j exp(s_j)
+ * with k_j, v_j the kv head h / G of position j, read through block_tables.
+ * Runs the fused kernel and, when the plan split a KV range, the combine
+ * kernel, both on `stream`.  The caches must already hold this step's K/V
+ * (mcp_paged_kv_append earlier on the same stream).
+ *
+ * q        device bf16 [T, H_q, D]
+ * k_cache, v_cache device bf16 [num_pages, P, H_kv, D]
+ * block_tables, cu_seqlens_q, seqlens_k: DEVICE copies of the metadata the
+ *          plan was built from (same values).
+ * out      device bf16 [T, H_q, D]  (rounded to nearest even from fp32)
+ * lse      device float32 [T, H_q], or NULL
+ * workspace: the one the plan was uploaded into.
+ * Rows of segments with Lq = 0 do not exist; no other output row is skipped.
+ */
+mcp_status mcp_mixed_attn_fwd(const mcp_plan* plan, const void* q, const void* k_cache,
+                              const void* v_cache, const int32_t* block_tables,
+                              const int32_t* cu_seqlens_q, const int32_t* seqlens_k, void* out,
+                              float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, read the device error word of `workspace` (the one
+ * mcp_mixed_attn_fwd and the plan's kernels write; or any int32 error word
+ * given to mcp_paged_kv_append) and clear it.  Returns MCP_OK,
+ * MCP_ERR_TIMEOUT (a bounded device wait gave up) or MCP_ERR_DEVICE_CHECK
+ * (an out-of-range page or slot was skipped).
+ */
+mcp_status mcp_check_device_errors(int32_t* error_word, void* stream);
+
+/* Device address of the error word inside a workspace laid out by `plan`. */
+int32_t* mcp_workspace_error_word(const mcp_plan* plan, void* workspace);
+
+/* ------------------------------------------------------------------------- */
+/* a8 standalone: merge split attention states                               */
+/* ------------------------------------------------------------------------- */
+/*
+ * Merge n attention results over disjoint key sets (split-KV): for each row r
+ * and head h, with M = max_k lse[k,r,h] and w_k = exp(lse[k,r,h] - M),
+ *   out[r,h,:] = sum_k w_k o[k,r,h,:] / sum_k w_k,  lse_out = M + ln sum_k w_k.
+ * A part with lse = -inf carries weight 0.  Not on the pages: it is the plain
+ * identity that makes split-KV equal to unsplit attention.
+ *
+ * o_parts   device float32 [n, rows, heads, head_dim], each part normalised
+ * lse_parts device float32 [n, rows, heads]
+ * out       device bf16 [rows, heads, head_dim];  lse_out float32 or NULL
+ */
+mcp_status mcp_merge_states(const float* o_parts, const float* lse_parts, int32_t n, int32_t rows,
+                            int32_t heads, int32_t head_dim, void* out, float* lse_out,
+                            void* stream);
+
+/* Device-check bits written to an error word. */
+#define MCP_DEVERR_TIMEOUT 0x1      /* a bounded mbarrier wait gave up           */
+#define MCP_DEVERR_PAGE_RANGE 0x2   /* a block-table page id outside the pool    */
+#define MCP_DEVERR_SLOT_RANGE 0x4   /* an append slot outside the pool           */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MCP_H_ */

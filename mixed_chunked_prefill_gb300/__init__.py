@@ -1,0 +1,183 @@
+"""Mixed chunked-prefill + decode paged attention for GB300 (sm_103a).
+
+Python binding of the C ABI in ``include/mcp.h``.  The functions here only
+check and marshal arguments (torch tensors -> device pointers, the current
+CUDA stream); every step of the computation runs in the library's CUDA
+kernels.  If the library is not built, every call raises: there is no CPU or
+PyTorch fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import _capi
+from ._capi import (  # noqa: F401
+    DEVERR_PAGE_RANGE,
+    DEVERR_SLOT_RANGE,
+    DEVERR_TIMEOUT,
+    AttnDesc,
+    MCPError,
+    Plan,
+    PlanOptions,
+)
+
+__all__ = [
+    "AttnDesc", "Plan", "PlanOptions", "MCPError", "load", "abi_version", "paged_kv_append",
+    "build_slot_mapping", "mixed_attn_plan", "mixed_attn_fwd", "check_device_errors",
+    "workspace_error_word", "merge_states", "make_desc",
+]
+
+
+def load():
+    return _capi.load()
+
+
+def abi_version() -> int:
+    return int(load().mcp_abi_version())
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if hasattr(stream, "cuda_stream"):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev(t, dtype, name):
+    import torch
+
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_i32(a, name):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def make_desc(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, page_size,
+              max_pages_per_seq, num_pages, sm_scale) -> AttnDesc:
+    return AttnDesc(int(num_seqs), int(total_q), int(num_q_heads), int(num_kv_heads),
+                    int(head_dim), int(page_size), int(max_pages_per_seq), int(num_pages),
+                    float(sm_scale))
+
+
+def paged_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, error_word=None, stream=None):
+    """Scatter k_new/v_new [T, H_kv, D] (bf16) into the paged caches
+    [num_pages, P, H_kv, D] at slot_mapping [T] (int64; < 0 skips).
+    ``error_word``: None, an int32 CUDA tensor, or a device address."""
+    import torch
+
+    lib = load()
+    T = int(k_new.shape[0]) if k_new.dim() > 0 else 0
+    num_pages, P, Hkv, D = (int(x) for x in k_cache.shape)
+    if tuple(k_new.shape) != (T, Hkv, D) or tuple(v_new.shape) != (T, Hkv, D):
+        raise ValueError("k_new / v_new must be [T, H_kv, D] matching the cache")
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache shapes differ")
+    if tuple(slot_mapping.shape) != (T,):
+        raise ValueError("slot_mapping must be [T]")
+    if error_word is None or isinstance(error_word, torch.Tensor):
+        ew = _dev(error_word, torch.int32, "error_word")
+    else:  # a device address, e.g. workspace_error_word(plan, workspace)
+        ew = ctypes.c_void_p(int(error_word))
+    st = lib.mcp_paged_kv_append(
+        _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(slot_mapping, torch.int64, "slot_mapping"), T, Hkv, D, P, num_pages,
+        _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
+        ew, _stream(stream))
+    _capi.check(st, "paged_kv_append")
+
+
+def build_slot_mapping(block_tables, cu_seqlens_q, seqlens_k, page_size, num_pages) -> np.ndarray:
+    """Host-side slot mapping of the step's new tokens (int64 numpy array)."""
+    lib = load()
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    S = bt.shape[0]
+    cu, cu_p = _host_i32(cu_seqlens_q, "cu_seqlens_q")
+    sk, sk_p = _host_i32(seqlens_k, "seqlens_k")
+    out = np.empty(int(cu[-1]), dtype=np.int64)
+    st = lib.mcp_build_slot_mapping(bt.ctypes.data_as(ctypes.c_void_p), S,
+                                    bt.shape[1] if bt.ndim == 2 else 0, int(page_size),
+                                    int(num_pages), cu_p, sk_p,
+                                    out.ctypes.data_as(ctypes.c_void_p))
+    _capi.check(st, "build_slot_mapping")
+    return out
+
+
+def mixed_attn_plan(desc: AttnDesc, cu_seqlens_q, seqlens_k, options: PlanOptions | None = None,
+                    workspace=None, stream=None) -> Plan:
+    """Plan a step from HOST metadata; with ``workspace`` (uint8 CUDA tensor)
+    also copy the work lists into it."""
+    import torch
+
+    lib = load()
+    cu, cu_p = _host_i32(cu_seqlens_q, "cu_seqlens_q")
+    sk, sk_p = _host_i32(seqlens_k, "seqlens_k")
+    plan = Plan()
+    ws = _dev(workspace, torch.uint8, "workspace") if workspace is not None else None
+    nbytes = int(workspace.numel()) if workspace is not None else 0
+    st = lib.mcp_mixed_attn_plan(ctypes.byref(desc), cu_p, sk_p,
+                                 ctypes.byref(options) if options is not None else None,
+                                 ctypes.byref(plan), ws, nbytes,
+                                 _stream(stream) if workspace is not None else None)
+    _capi.check(st, "mixed_attn_plan")
+    return plan
+
+
+def mixed_attn_fwd(plan: Plan, q, k_cache, v_cache, block_tables, cu_seqlens_q, seqlens_k, out,
+                   lse=None, workspace=None, stream=None) -> None:
+    """Fused mixed attention forward on device tensors (see include/mcp.h)."""
+    import torch
+
+    lib = load()
+    st = lib.mcp_mixed_attn_fwd(
+        ctypes.byref(plan), _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),
+        _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _dev(seqlens_k, torch.int32, "seqlens_k"),
+        _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse"),
+        _dev(workspace, torch.uint8, "workspace"),
+        int(workspace.numel()) if workspace is not None else 0, _stream(stream))
+    _capi.check(st, "mixed_attn_fwd")
+
+
+def workspace_error_word(plan: Plan, workspace) -> int:
+    lib = load()
+    return int(lib.mcp_workspace_error_word(ctypes.byref(plan), ctypes.c_void_p(workspace.data_ptr())))
+
+
+def check_device_errors(error_word_ptr: int, stream=None) -> None:
+    """Synchronise, read and clear a device error word; raise on a set bit."""
+    lib = load()
+    st = lib.mcp_check_device_errors(ctypes.c_void_p(int(error_word_ptr)), _stream(stream))
+    _capi.check(st, "check_device_errors")
+
+
+def merge_states(o_parts, lse_parts, out, lse_out=None, stream=None) -> None:
+    """Merge split attention states: o_parts [n, R, H, D] fp32, lse_parts [n, R, H]."""
+    import torch
+
+    lib = load()
+    n, R, H, D = (int(x) for x in o_parts.shape)
+    if tuple(lse_parts.shape) != (n, R, H) or tuple(out.shape) != (R, H, D):
+        raise ValueError("shape mismatch")
+    st = lib.mcp_merge_states(_dev(o_parts, torch.float32, "o_parts"),
+                              _dev(lse_parts, torch.float32, "lse_parts"), n, R, H, D,
+                              _dev(out, torch.bfloat16, "out"),
+                              _dev(lse_out, torch.float32, "lse_out"), _stream(stream))
+    _capi.check(st, "merge_states")

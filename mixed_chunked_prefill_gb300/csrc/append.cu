@@ -1,0 +1,62 @@
+// Paged KV append: scatter each new token's K/V row into its physical slot.
+//
+// [W] "输入组装": the new tokens' K/V are written into the paged cache through
+// slot_mapping before attention runs; [L] 4.2 (append_paged_kv_cache):
+// physical-address translation and scattered (non-contiguous) writes.
+// Slots are distinct within one call, so plain stores suffice.
+//
+// HBM-bound copy: each token row is H_kv * D * 2 bytes, moved as 16-byte
+// vectors; consecutive threads take consecutive vectors of a row, so both the
+// read of k_new / v_new and the write into the page are coalesced.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mcp.h"
+#include "mcp_internal.h"
+
+namespace mcp {
+namespace {
+
+__global__ void __launch_bounds__(256) paged_kv_append_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+    const int64_t* __restrict__ slots, int64_t total_vec, int32_t vec_per_tok, int64_t num_slots,
+    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int32_t* err) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vec;
+       i += stride) {
+    const int64_t t = i / vec_per_tok;
+    const int64_t c = i - t * vec_per_tok;
+    const int64_t slot = slots[t];
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (err && c == 0) atomicOr(err, MCP_DEVERR_SLOT_RANGE);
+      continue;
+    }
+    const int64_t dst = slot * vec_per_tok + c;
+    k_cache[dst] = k_new[i];
+    v_cache[dst] = v_new[i];
+  }
+}
+
+}  // namespace
+
+int launch_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                  int32_t num_tokens, int32_t row_bytes, int64_t num_slots, void* k_cache,
+                  void* v_cache, int32_t* error_word, void* stream) {
+  if (num_tokens <= 0) return 0;
+  const int32_t vec_per_tok = row_bytes / 16;
+  const int64_t total = static_cast<int64_t>(num_tokens) * vec_per_tok;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  if (blocks > cap) blocks = cap;
+  paged_kv_append_kernel<<<static_cast<int>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, total,
+      vec_per_tok, num_slots, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+      error_word);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace mcp

@@ -1,0 +1,819 @@
+// Fused mixed (chunked-prefill + decode) paged-attention forward for sm_103a.
+//
+// One launch serves the whole packed token stream ([K] "平铺策略 / 掩码特化":
+// one kernel for prefill chunks and decodes; [W] "Flash Attention 的 varlen
+// 接口": the i-th query segment attends only to the i-th KV segment,
+// right-aligned causal).  Each CTA runs one work item from the host plan:
+//
+//  * prefill item -- 128 query rows (the G query heads of one kv head packed
+//    with 128/G tokens) against a KV range in 128-key tiles.  Warp 0 issues TMA
+//    page loads (8 pages x 16 tokens per tile, each page through the block
+//    table), warp 1 issues tcgen05.mma (S = Q K^T into TMEM, O += P V into
+//    TMEM), warps 2-5 run the online softmax on S rows read from TMEM, write P
+//    (bf16) to shared memory and rescale O lazily.  Only tiles that straddle
+//    the diagonal are masked ([K] "掩码特化").
+//  * decode item -- the G*Lq (<= 16) query rows of one kv head against a KV
+//    range, page by page: warp 0 streams K/V pages with TMA into a 16-stage
+//    ring, warps 2-5 each take every 4th page (ldmatrix + mma.sync m16n8k16,
+//    quad-shuffle max/sum, online softmax) and merge their states at the end.
+//
+// A split KV range writes (O, LSE) partials that combine.cu merges.
+//
+// Every mbarrier wait is bounded in time.  On time-out the CTA records
+// MCP_DEVERR_TIMEOUT in the error word, every role leaves its loop, in-flight
+// TMA copies and MMAs are drained (again with a bound), TMEM is freed and the
+// CTA exits without writing outputs.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "mcp.h"
+#include "mcp_internal.h"
+#include "ptx.cuh"
+
+namespace mcp {
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per wait
+constexpr float kRescaleThreshold = 8.0f;  // rescale O only when the max grows by > 2^8
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kLog2e = 1.44269504088896341f;
+constexpr int kDecStages = 16;  // decode page ring depth
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+template <int D>
+struct Cfg {
+  static constexpr int kHalves = D / 64;         // 64-column (128-byte) swizzle panels
+  static constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 B
+  // prefill
+  static constexpr int kQBytes = kHalves * kHalfBytes;
+  static constexpr int kKvBytes = kHalves * kHalfBytes;  // one K (or V) tile of 128 keys
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kQBytes;                  // stage s: K at kOffK + 2*s*kKvBytes, V after
+  static constexpr int kOffP = kOffK + 4 * kKvBytes;
+  static constexpr int kPBytes = 2 * kHalfBytes;         // P: 128 rows x 128 keys bf16
+  static constexpr int kPrefillBytes = kOffP + kPBytes;
+  // decode
+  static constexpr int kPageBytes = kHalves * kPageSize * 128;  // one page of one kv head
+  static constexpr int kStageBytes = 2 * kPageBytes;            // K page + V page
+  static constexpr int kOffRing = 0;
+  static constexpr int kOffMerge = kDecStages * kStageBytes;
+  static constexpr int kMergeBytes = 4 * 16 * D * 4 + 2 * 64 * 4;
+  static constexpr int kDecodeBytes = kOffMerge + kMergeBytes;
+  // common
+  static constexpr int kDataBytes = kPrefillBytes > kDecodeBytes ? kPrefillBytes : kDecodeBytes;
+  static constexpr int kOffBar = (kDataBytes + 1023) & ~1023;
+  static constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // barriers/flags + alignment slack
+};
+
+// barrier slots
+enum : int {
+  BQ = 0,       // Q tile landed
+  BK0 = 1,      // K tile of stage s landed (BK0 + s)
+  BV0 = 3,      // V tile of stage s landed
+  BE0 = 5,      // stage s free again (MMA done with K and V)
+  BS0 = 7,      // S buffer s holds Q K^T of the current tile
+  BP = 9,       // P of the current tile written (128 softmax threads)
+  BPV = 10,     // P V of the current tile accumulated into O
+  BDRAIN = 11,  // all MMAs of the CTA finished
+  BFULL0 = 16,  // decode ring stage landed
+  BEMPTY0 = 32, // decode ring stage free
+  kNumBars = 48
+};
+
+struct Ctx {
+  uint32_t bar;
+  volatile int* abort;
+  int32_t* err;
+  __device__ __forceinline__ uint32_t b(int i) const { return bar + 8u * static_cast<uint32_t>(i); }
+};
+
+// Wait for the phase with `parity` of barrier `bar` to complete; false if the
+// CTA aborted or the wait ran past kWaitLimitNs (then the CTA aborts).
+__device__ __noinline__ bool wait_on(const Ctx& c, uint32_t bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+#pragma unroll 1
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*c.abort) return false;
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *c.abort = 1;
+      if (c.err) atomicOr(c.err, MCP_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used to let this CTA's own async
+// copies / MMAs finish before it exits.
+__device__ __noinline__ void drain_wait(const Ctx& c, uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+#pragma unroll 1
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *c.abort = 1;
+      if (c.err) atomicOr(c.err, MCP_DEVERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+struct KParams {
+  const WorkItem* items;
+  const int32_t* cu_q;
+  const int32_t* seqlens_k;
+  const int32_t* bt;
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  int32_t* err;
+  int32_t max_pages;
+  int32_t num_pages;
+  int32_t hq;
+  int32_t G;
+  float scale_log2;  // sm_scale * log2(e): scores live in log2 units
+};
+
+struct Seg {
+  int q_start, lq, lk, hist;
+};
+
+// Physical page of logical page `lp` of segment `seg`, or num_pages (an
+// out-of-range TMA coordinate: the copy fills zeros) with an error bit when
+// the block table names a page outside the pool.
+__device__ __forceinline__ int page_of(const KParams& p, int seg, int lp) {
+  const int v = p.bt[static_cast<size_t>(seg) * p.max_pages + lp];
+  if (v >= 0 && v < p.num_pages) return v;
+  atomicOr(p.err, MCP_DEVERR_PAGE_RANGE);
+  return p.num_pages;
+}
+
+// ------------------------------------------------------------------------
+// prefill item: tcgen05 tile
+// ------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, const Seg& sg,
+                                             const KParams& p, uint32_t base, uint8_t* gb,
+                                             uint32_t tmem, const CUtensorMap* tm_q,
+                                             const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                             int warp, int lane) {
+  using C = Cfg<D>;
+  const int G = p.G;
+  const int TQ = kTileRows / G;
+  const int kv0 = it.kv_begin, kv1 = it.kv_end;
+  const int ntiles = (kv1 - kv0 + kKvTile - 1) / kKvTile;
+  const uint32_t sQ = base + C::kOffQ;
+  const uint32_t sP = base + C::kOffP;
+  auto sK = [&](int s) { return base + C::kOffK + static_cast<uint32_t>(2 * s * C::kKvBytes); };
+  auto sV = [&](int s) { return sK(s) + C::kKvBytes; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    const uint64_t pol_q = ptx::policy_evict_first();
+    const uint64_t pol_kv = ptx::policy_evict_last();  // other q tiles re-read these K/V
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(c.b(BQ), C::kHalves * G * TQ * 128);
+      for (int h = 0; h < C::kHalves; ++h)
+        ptx::tma_load_4d(sQ + h * C::kHalfBytes, tm_q, c.b(BQ), 0, h, it.kv_head * G,
+                         sg.q_start + it.q_begin, pol_q);
+    }
+    int t = 0;
+    for (; t < ntiles; ++t) {
+      const int s = t & 1;
+      if (t >= 2 && !wait_on(c, c.b(BE0 + s), ((t >> 1) + 1) & 1)) break;
+      const int key0 = kv0 + t * kKvTile;
+      int npg = (kv1 - key0 + kPageSize - 1) / kPageSize;
+      npg = npg < kKvTile / kPageSize ? npg : kKvTile / kPageSize;
+      const int pg = lane < npg ? page_of(p, it.seg, key0 / kPageSize + lane) : p.num_pages;
+      int pgs[kKvTile / kPageSize];
+#pragma unroll
+      for (int i = 0; i < kKvTile / kPageSize; ++i) pgs[i] = __shfl_sync(0xffffffffu, pg, i);
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(c.b(BK0 + s), C::kKvBytes);
+#pragma unroll
+        for (int i = 0; i < kKvTile / kPageSize; ++i)
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h)
+            ptx::tma_load_5d(sK(s) + h * C::kHalfBytes + i * kPageSize * 128, tm_k, c.b(BK0 + s),
+                             0, h, it.kv_head, 0, pgs[i], pol_kv);
+        ptx::mbar_arrive_expect_tx(c.b(BV0 + s), C::kKvBytes);
+#pragma unroll
+        for (int i = 0; i < kKvTile / kPageSize; ++i)
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h)
+            ptx::tma_load_5d(sV(s) + h * C::kHalfBytes + i * kPageSize * 128, tm_v, c.b(BV0 + s),
+                             0, h, it.kv_head, 0, pgs[i], pol_kv);
+      }
+      __syncwarp();
+    }
+    // drain: the last tile issued into each stage, and Q
+    for (int s = 0; s < 2; ++s) {
+      const int last = (t - 1 - s) >= 0 ? (t - 1 - ((t - 1 - s) & 1)) : -1;
+      if (last >= 0) {
+        drain_wait(c, c.b(BK0 + s), (last >> 1) & 1);
+        drain_wait(c, c.b(BV0 + s), (last >> 1) & 1);
+      }
+    }
+    drain_wait(c, c.b(BQ), 0);
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    constexpr uint32_t kIdQK = ptx::idesc_bf16(128, kKvTile, false);
+    constexpr uint32_t kIdPV = ptx::idesc_bf16(128, D, true);
+    const uint32_t tS = tmem;        // S buffers: columns [0,128) and [128,256)
+    const uint32_t tO = tmem + 256;  // O: columns [256, 256 + D)
+    bool issued = false;
+    auto qk = [&](int t) -> bool {
+      const int s = t & 1;
+      if (!wait_on(c, c.b(BK0 + s), (t >> 1) & 1)) return false;
+      ptx::tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+          ptx::mma_ss(tS + s * kKvTile, ptx::sdesc_sw128(sQ + off, 16, 1024),
+                      ptx::sdesc_sw128(sK(s) + off, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(c.b(BS0 + s));
+      }
+      __syncwarp();
+      issued = true;
+      return true;
+    };
+    bool ok = wait_on(c, c.b(BQ), 0);
+    if (ok) ok = qk(0);
+    for (int t = 0; ok && t < ntiles; ++t) {
+      if (t + 1 < ntiles && !(ok = qk(t + 1))) break;
+      if (!(ok = wait_on(c, c.b(BP), t & 1))) break;
+      const int s = t & 1;
+      if (!(ok = wait_on(c, c.b(BV0 + s), (t >> 1) & 1))) break;
+      const int nval = kv1 - (kv0 + t * kKvTile);
+      if (nval < kKvTile && (nval & (kPageSize - 1))) {
+        // Rows past the item's last key inside its last page may be unused
+        // cache slots holding anything (NaN included); P is 0 there but
+        // 0 * NaN would reach O, so those V rows are zeroed.
+        const int r0 = nval, nr = ((nval + kPageSize - 1) & ~(kPageSize - 1)) - nval;
+        const int per_half = nr * 8;
+        uint8_t* gV = gb + (sV(s) - base);
+        for (int i = lane; i < per_half * C::kHalves; i += 32) {
+          const int h = i / per_half, rem = i - h * per_half;
+          const int r = r0 + rem / 8, ch = rem & 7;
+          *reinterpret_cast<uint4*>(gV + h * C::kHalfBytes + r * 128 + ch * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+      }
+      ptx::tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < kKvTile / 16; ++kk) {
+          ptx::mma_ss(tO,
+                      ptx::sdesc_sw128(sP + (kk >> 2) * C::kHalfBytes + (kk & 3) * 32, 16, 1024),
+                      ptx::sdesc_sw128(sV(s) + kk * 16 * 128, C::kHalfBytes, 1024), kIdPV,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(c.b(BPV));
+        ptx::mma_commit(c.b(BE0 + s));
+      }
+      __syncwarp();
+    }
+    if (issued) {
+      if (lane == 0) ptx::mma_commit(c.b(BDRAIN));
+      __syncwarp();
+      drain_wait(c, c.b(BDRAIN), 0);
+    }
+  } else {
+    // ------------------------------------------- softmax + epilogue (2-5)
+    const int qw = warp & 3;
+    const int row = qw * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
+    const uint32_t tS = tmem + lane_base;
+    const uint32_t tO = tmem + 256 + lane_base;
+    const int tok = it.q_begin + row / G;  // token index inside the segment
+    const int g = row - (row / G) * G;
+    const bool valid = row < G * TQ && tok < it.q_begin + it.q_count;
+    const int tok_c = tok < it.q_begin + it.q_count ? tok : it.q_begin + it.q_count - 1;
+    // right-aligned causal: token i sees keys 0 .. hist + i; the item covers keys < kv1
+    int jmax = sg.hist + tok_c;
+    jmax = jmax < kv1 - 1 ? jmax : kv1 - 1;
+    const float sl2 = p.scale_log2;
+    uint8_t* gP = gb + C::kOffP;
+    float m_ref = neg_inf(), l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = t & 1;
+      if (!(ok = wait_on(c, c.b(BS0 + s), (t >> 1) & 1))) break;
+      ptx::tc_fence_after();
+      uint32_t r[kKvTile];
+#pragma unroll
+      for (int j = 0; j < kKvTile / 32; ++j) ptx::tmem_ld32(tS + s * kKvTile + j * 32, r + j * 32);
+      ptx::tmem_wait_ld();
+      const int key0 = kv0 + t * kKvTile;
+      float mx = neg_inf();
+      if (key0 + kKvTile - 1 <= jmax) {  // every key of the tile is visible to this row
+#pragma unroll
+        for (int i = 0; i < kKvTile; ++i) {
+          const float x = __uint_as_float(r[i]) * sl2;
+          r[i] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+      } else {  // diagonal / last tile: mask keys past this row's last visible key
+#pragma unroll
+        for (int i = 0; i < kKvTile; ++i) {
+          const float x = (key0 + i <= jmax) ? __uint_as_float(r[i]) * sl2 : neg_inf();
+          r[i] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+      }
+      const float m_new = fmaxf(m_ref, mx);
+      const bool rescale = m_new > m_ref + kRescaleThreshold;
+      float alpha = 1.f;
+      if (rescale) {
+        alpha = ptx::ex2(m_ref - m_new);
+        m_ref = m_new;
+      }
+      const float m_use = m_ref == neg_inf() ? 0.f : m_ref;
+      float sum = 0.f;
+      uint32_t pk[kKvTile / 2];
+#pragma unroll
+      for (int i = 0; i < kKvTile; i += 2) {
+        const float p0 = ptx::ex2(__uint_as_float(r[i]) - m_use);
+        const float p1 = ptx::ex2(__uint_as_float(r[i + 1]) - m_use);
+        sum += p0 + p1;
+        pk[i / 2] = ptx::pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + sum;
+      if (t > 0) {
+        // P V of the previous tile must be done before O is rescaled and P overwritten
+        if (!(ok = wait_on(c, c.b(BPV), (t - 1) & 1))) break;
+        ptx::tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int j = 0; j < D / 32; ++j) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + j * 32, o);
+            ptx::tmem_wait_ld();
+            if (rescale) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            }
+            ptx::tmem_st32(tO + j * 32, o);
+          }
+          ptx::tmem_wait_st();
+        }
+      }
+      // P row -> shared memory, K-major with the 128-byte swizzle: keys
+      // [64h, 64h + 64) of this row in panel h, 16-byte chunk j at j ^ (row & 7)
+#pragma unroll
+      for (int ch = 0; ch < kKvTile / 8; ++ch) {
+        const int h = ch >> 3, cc = ch & 7;
+        *reinterpret_cast<uint4*>(gP + h * C::kHalfBytes + row * 128 + ((cc ^ (row & 7)) << 4)) =
+            make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.b(BP));
+    }
+    if (ok && ntiles > 0) ok = wait_on(c, c.b(BPV), (ntiles - 1) & 1);
+    ptx::tc_fence_after();
+    const bool store = ok && valid && !*c.abort;
+    const bool direct = it.part_row < 0;
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const size_t orow = static_cast<size_t>(sg.q_start + tok) * p.hq + it.kv_head * G + g;
+#pragma unroll 1
+    for (int j = 0; j < D / 32; ++j) {
+      uint32_t o[32];
+      ptx::tmem_ld32(tO + j * 32, o);
+      ptx::tmem_wait_ld();
+      if (store) {
+        if (direct) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + j * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            dst[v] = make_uint4(
+                ptx::pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
+                ptx::pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l),
+                ptx::pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l),
+                ptx::pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l));
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(
+              p.part_o + static_cast<size_t>(it.part_row + row) * D + j * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        }
+      }
+    }
+    if (store) {
+      const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : neg_inf();
+      if (direct) {
+        if (p.lse) p.lse[orow] = lse;
+      } else {
+        p.part_lse[it.part_row + row] = lse;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------
+// decode item: TMA page ring + mma.sync
+// ------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t keep_pair(uint32_t v, int k, int nvalid) {
+  const uint32_t lo = k < nvalid ? 0x0000FFFFu : 0u;
+  const uint32_t hi = k + 1 < nvalid ? 0xFFFF0000u : 0u;
+  return v & (lo | hi);
+}
+
+template <int D>
+__device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, const Seg& sg,
+                                            const KParams& p, uint32_t base, uint8_t* gb,
+                                            const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                            int warp, int lane) {
+  using C = Cfg<D>;
+  const int G = p.G;
+  const int kv0 = it.kv_begin, kv1 = it.kv_end;
+  const int npg = (kv1 - kv0 + kPageSize - 1) / kPageSize;
+  const uint32_t ring = base + C::kOffRing;
+
+  if (warp == 0) {
+    const uint64_t pol = ptx::policy_evict_first();  // each page is read once
+    int issued = 0;
+    bool ok = true;
+    for (int b0 = 0; ok && b0 < npg; b0 += 32) {
+      const int n = npg - b0 < 32 ? npg - b0 : 32;
+      const int pg = lane < n ? page_of(p, it.seg, kv0 / kPageSize + b0 + lane) : p.num_pages;
+      for (int i = 0; i < n; ++i) {
+        const int pi = b0 + i;
+        const int s = pi % kDecStages;
+        if (pi >= kDecStages && !(ok = wait_on(c, c.b(BEMPTY0 + s), ((pi / kDecStages) + 1) & 1)))
+          break;
+        const int pgi = __shfl_sync(0xffffffffu, pg, i);
+        if (lane == 0) {
+          const uint32_t dst = ring + s * C::kStageBytes;
+          ptx::mbar_arrive_expect_tx(c.b(BFULL0 + s), C::kStageBytes);
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h)
+            ptx::tma_load_5d(dst + h * kPageSize * 128, tm_k, c.b(BFULL0 + s), 0, h, it.kv_head, 0,
+                             pgi, pol);
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h)
+            ptx::tma_load_5d(dst + C::kPageBytes + h * kPageSize * 128, tm_v, c.b(BFULL0 + s), 0,
+                             h, it.kv_head, 0, pgi, pol);
+        }
+        __syncwarp();
+        issued = pi + 1;
+      }
+    }
+    for (int s = 0; s < kDecStages && s < issued; ++s) {
+      const int last = s + ((issued - 1 - s) / kDecStages) * kDecStages;
+      drain_wait(c, c.b(BFULL0 + s), (last / kDecStages) & 1);
+    }
+  } else if (warp >= 2) {
+    const int cw = warp - 2;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int R = it.q_count * G;
+    const int last_tok = it.q_count - 1;
+    const int tl = gid / G < last_tok ? gid / G : last_tok;
+    const int th = (gid + 8) / G < last_tok ? (gid + 8) / G : last_tok;
+    const int jlo = min(sg.hist + it.q_begin + tl, kv1 - 1);
+    const int jhi = min(sg.hist + it.q_begin + th, kv1 - 1);
+    const bool vlo = gid < R, vhi = gid + 8 < R;
+    const float sl2 = p.scale_log2;
+
+    // Q rows (row r = token r / G, head r % G of this kv head) as m16n8k16 A fragments
+    uint32_t qa[D / 16][4];
+    {
+      const uint32_t* qlo = reinterpret_cast<const uint32_t*>(
+          p.q + (static_cast<size_t>(sg.q_start + it.q_begin + gid / G) * p.hq + it.kv_head * G +
+                 gid % G) * D);
+      const uint32_t* qhi = reinterpret_cast<const uint32_t*>(
+          p.q + (static_cast<size_t>(sg.q_start + it.q_begin + (gid + 8) / G) * p.hq +
+                 it.kv_head * G + (gid + 8) % G) * D);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        qa[kk][0] = vlo ? qlo[kk * 8 + tig] : 0u;
+        qa[kk][1] = vhi ? qhi[kk * 8 + tig] : 0u;
+        qa[kk][2] = vlo ? qlo[kk * 8 + 4 + tig] : 0u;
+        qa[kk][3] = vhi ? qhi[kk * 8 + 4 + tig] : 0u;
+      }
+    }
+    float o[D / 8][4];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float mlo = neg_inf(), mhi = neg_inf(), llo = 0.f, lhi = 0.f;
+    bool ok = true;
+    const int mi = lane >> 3, rr = lane & 7;
+    for (int pi = cw; pi < npg; pi += 4) {
+      const int s = pi % kDecStages;
+      if (!(ok = wait_on(c, c.b(BFULL0 + s), (pi / kDecStages) & 1))) break;
+      const uint32_t kb = ring + s * C::kStageBytes;
+      const uint32_t vb = kb + C::kPageBytes;
+      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int h = kk >> 2, c0 = (kk & 3) * 2;
+        const int tk = (mi >> 1) * 8 + rr;  // matrices: (tok 0-7, c0) (0-7, c0+1) (8-15, c0) (8-15, c0+1)
+        const int ch = c0 + (mi & 1);
+        uint32_t b0, b1, b2, b3;
+        ptx::ldsm_x4(kb + h * kPageSize * 128 + tk * 128 + ((ch ^ (tk & 7)) << 4), b0, b1, b2, b3);
+        ptx::mma16816(sacc[0], qa[kk], b0, b1);
+        ptx::mma16816(sacc[1], qa[kk], b2, b3);
+      }
+      const int key0 = kv0 + pi * kPageSize;
+      float x[2][4];
+      float xlo = neg_inf(), xhi = neg_inf();
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = key0 + nt * 8 + tig * 2 + e;
+          x[nt][e] = key <= jlo ? sacc[nt][e] * sl2 : neg_inf();
+          x[nt][2 + e] = key <= jhi ? sacc[nt][2 + e] * sl2 : neg_inf();
+          xlo = fmaxf(xlo, x[nt][e]);
+          xhi = fmaxf(xhi, x[nt][2 + e]);
+        }
+      xlo = fmaxf(xlo, __shfl_xor_sync(0xffffffffu, xlo, 1));
+      xlo = fmaxf(xlo, __shfl_xor_sync(0xffffffffu, xlo, 2));
+      xhi = fmaxf(xhi, __shfl_xor_sync(0xffffffffu, xhi, 1));
+      xhi = fmaxf(xhi, __shfl_xor_sync(0xffffffffu, xhi, 2));
+      const float nlo = fmaxf(mlo, xlo), nhi = fmaxf(mhi, xhi);
+      if (nlo > mlo + kRescaleThreshold) {
+        const float a = ptx::ex2(mlo - nlo);
+        mlo = nlo;
+        llo *= a;
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) { o[i][0] *= a; o[i][1] *= a; }
+      }
+      if (nhi > mhi + kRescaleThreshold) {
+        const float a = ptx::ex2(mhi - nhi);
+        mhi = nhi;
+        lhi *= a;
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) { o[i][2] *= a; o[i][3] *= a; }
+      }
+      const float ulo = mlo == neg_inf() ? 0.f : mlo;
+      const float uhi = mhi == neg_inf() ? 0.f : mhi;
+      float pv[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        pv[nt][0] = ptx::ex2(x[nt][0] - ulo);
+        pv[nt][1] = ptx::ex2(x[nt][1] - ulo);
+        pv[nt][2] = ptx::ex2(x[nt][2] - uhi);
+        pv[nt][3] = ptx::ex2(x[nt][3] - uhi);
+        llo += pv[nt][0] + pv[nt][1];
+        lhi += pv[nt][2] + pv[nt][3];
+      }
+      uint32_t pa[4] = {ptx::pack_bf16x2(pv[0][0], pv[0][1]), ptx::pack_bf16x2(pv[0][2], pv[0][3]),
+                        ptx::pack_bf16x2(pv[1][0], pv[1][1]), ptx::pack_bf16x2(pv[1][2], pv[1][3])};
+      const int nvalid = kv1 - key0;
+#pragma unroll
+      for (int dd = 0; dd < D / 16; ++dd) {
+        const int h = dd >> 2, c0 = (dd & 3) * 2;
+        const int tk = (mi & 1) * 8 + rr;  // matrices: (tok 0-7, c0) (8-15, c0) (0-7, c0+1) (8-15, c0+1)
+        const int ch = c0 + (mi >> 1);
+        uint32_t v0, v1, v2, v3;
+        ptx::ldsm_x4_t(vb + h * kPageSize * 128 + tk * 128 + ((ch ^ (tk & 7)) << 4), v0, v1, v2, v3);
+        if (nvalid < kPageSize) {
+          // keys past the item's end: unused slots may hold NaN; P is 0 there
+          v0 = keep_pair(v0, tig * 2, nvalid);
+          v1 = keep_pair(v1, 8 + tig * 2, nvalid);
+          v2 = keep_pair(v2, tig * 2, nvalid);
+          v3 = keep_pair(v3, 8 + tig * 2, nvalid);
+        }
+        ptx::mma16816(o[2 * dd], pa, v0, v1);
+        ptx::mma16816(o[2 * dd + 1], pa, v2, v3);
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(c.b(BEMPTY0 + s));
+    }
+    // full row sums inside each quad
+    llo += __shfl_xor_sync(0xffffffffu, llo, 1);
+    llo += __shfl_xor_sync(0xffffffffu, llo, 2);
+    lhi += __shfl_xor_sync(0xffffffffu, lhi, 1);
+    lhi += __shfl_xor_sync(0xffffffffu, lhi, 2);
+    // merge the four warps' (m, l, O) through shared memory
+    float* mo = reinterpret_cast<float*>(gb + C::kOffMerge);
+    float* mm = mo + 4 * 16 * D;
+    float* ml = mm + 64;
+    float* mine = mo + cw * 16 * D;
+#pragma unroll
+    for (int nb = 0; nb < D / 8; ++nb) {
+      *reinterpret_cast<float2*>(mine + gid * D + nb * 8 + tig * 2) = make_float2(o[nb][0], o[nb][1]);
+      *reinterpret_cast<float2*>(mine + (gid + 8) * D + nb * 8 + tig * 2) = make_float2(o[nb][2], o[nb][3]);
+    }
+    if (tig == 0) {
+      mm[cw * 16 + gid] = mlo;
+      mm[cw * 16 + gid + 8] = mhi;
+      ml[cw * 16 + gid] = llo;
+      ml[cw * 16 + gid + 8] = lhi;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    const int t = threadIdx.x - 64;
+    const int row = t >> 3;
+    const int d0 = (t & 7) * (D / 8);
+    float M = neg_inf();
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, mm[w * 16 + row]);
+    float wt[4], L = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float mw = mm[w * 16 + row];
+      wt[w] = mw == neg_inf() ? 0.f : ptx::ex2(mw - M);
+      L += wt[w] * ml[w * 16 + row];
+    }
+    if (row < R && ok && !*c.abort) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      float acc[D / 8];
+#pragma unroll
+      for (int d = 0; d < D / 8; ++d) {
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) a += wt[w] * mo[w * 16 * D + row * D + d0 + d];
+        acc[d] = a * inv;
+      }
+      const int tok = it.q_begin + row / G;
+      const int g = row - (row / G) * G;
+      const size_t orow = static_cast<size_t>(sg.q_start + tok) * p.hq + it.kv_head * G + g;
+      const float lse = L > 0.f ? (M + log2f(L)) * kLn2 : neg_inf();
+      if (it.part_row < 0) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + orow * D + d0);
+#pragma unroll
+        for (int d = 0; d < D / 8; d += 8)
+          *reinterpret_cast<uint4*>(dst + d / 2) =
+              make_uint4(ptx::pack_bf16x2(acc[d], acc[d + 1]), ptx::pack_bf16x2(acc[d + 2], acc[d + 3]),
+                         ptx::pack_bf16x2(acc[d + 4], acc[d + 5]), ptx::pack_bf16x2(acc[d + 6], acc[d + 7]));
+        if (p.lse && (t & 7) == 0) p.lse[orow] = lse;
+      } else {
+        float* dst = p.part_o + static_cast<size_t>(it.part_row + row) * D + d0;
+#pragma unroll
+        for (int d = 0; d < D / 8; d += 4)
+          *reinterpret_cast<float4*>(dst + d) = make_float4(acc[d], acc[d + 1], acc[d + 2], acc[d + 3]);
+        if ((t & 7) == 0) p.part_lse[it.part_row + row] = lse;
+      }
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    mixed_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const KParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gb = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WorkItem it = p.items[blockIdx.x];
+  Ctx c;
+  c.bar = base + C::kOffBar;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + C::kOffBar + kNumBars * 8);
+  c.abort = reinterpret_cast<volatile int*>(gb + C::kOffBar + kNumBars * 8 + 16);
+  c.err = p.err;
+  const bool prefill = it.kind == kPrefillItem;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(c.b(i), 1);
+    ptx::mbar_init(c.b(BP), 128);
+    *c.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    if (prefill) ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+  }
+  if (prefill && warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+
+  Seg sg;
+  sg.q_start = p.cu_q[it.seg];
+  sg.lq = p.cu_q[it.seg + 1] - sg.q_start;
+  sg.lk = p.seqlens_k[it.seg];
+  sg.hist = sg.lk - sg.lq;
+
+  if (prefill) {
+    prefill_item<D>(c, it, sg, p, base, gb, *tmem_slot, &tm_q, &tm_k, &tm_v, warp, lane);
+  } else {
+    decode_item<D>(c, it, sg, p, base, gb, &tm_k, &tm_v, warp, lane);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (prefill && warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(*tmem_slot, 512);
+  }
+}
+
+// ------------------------------------------------------------------------
+// host side: tensor maps and launch
+// ------------------------------------------------------------------------
+thread_local char g_detail[256] = "";
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, const char* what) {
+  auto fn = encode_fn();
+  if (!fn) {
+    snprintf(g_detail, sizeof(g_detail), "cuTensorMapEncodeTiled unavailable");
+    return false;
+  }
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_detail, sizeof(g_detail), "tensor map for %s rejected (CUresult %d)", what, (int)r);
+    return false;
+  }
+  return true;
+}
+
+template <int D>
+int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
+  using C = Cfg<D>;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const int TQ = kTileRows / G;
+  alignas(64) CUtensorMap tq, tk, tv;
+  {
+    cuuint64_t dims[4] = {64, (cuuint64_t)(D / 64), (cuuint64_t)a.num_q_heads,
+                          (cuuint64_t)(a.total_q > 0 ? a.total_q : 1)};
+    cuuint64_t strides[3] = {128, (cuuint64_t)D * 2, (cuuint64_t)a.num_q_heads * D * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)G, (cuuint32_t)TQ};
+    if (!encode(&tq, a.q, 4, dims, strides, box, "q")) return -1;
+  }
+  {
+    cuuint64_t dims[5] = {64, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads,
+                          (cuuint64_t)a.page_size, (cuuint64_t)a.num_pages};
+    cuuint64_t strides[4] = {128, (cuuint64_t)D * 2, (cuuint64_t)a.num_kv_heads * D * 2,
+                             (cuuint64_t)a.page_size * a.num_kv_heads * D * 2};
+    cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)a.page_size, 1};
+    if (!encode(&tk, a.k_cache, 5, dims, strides, box, "k_cache")) return -1;
+    if (!encode(&tv, a.v_cache, 5, dims, strides, box, "v_cache")) return -1;
+  }
+  KParams kp;
+  kp.items = a.items;
+  kp.cu_q = a.cu_seqlens_q;
+  kp.seqlens_k = a.seqlens_k;
+  kp.bt = a.block_tables;
+  kp.q = static_cast<const __nv_bfloat16*>(a.q);
+  kp.out = static_cast<__nv_bfloat16*>(a.out);
+  kp.lse = a.lse;
+  kp.part_o = a.part_o;
+  kp.part_lse = a.part_lse;
+  kp.err = a.error_word;
+  kp.max_pages = a.max_pages_per_seq;
+  kp.num_pages = a.num_pages;
+  kp.hq = a.num_q_heads;
+  kp.G = G;
+  kp.scale_log2 = a.sm_scale * kLog2e;
+  cudaError_t e = cudaFuncSetAttribute(mixed_attn_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  mixed_attn_fwd_kernel<D><<<a.num_items, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, kp);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+
+const char* launch_detail() { return g_detail; }
+
+int launch_mixed_attn(const FwdArgs& a, void* stream) {
+  g_detail[0] = 0;
+  if (a.num_items <= 0) return 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (a.head_dim == 128) return launch_fwd_d<128>(a, st);
+  if (a.head_dim == 64) return launch_fwd_d<64>(a, st);
+  snprintf(g_detail, sizeof(g_detail), "head_dim %d not built", a.head_dim);
+  return -1;
+}
+
+}  // namespace mcp

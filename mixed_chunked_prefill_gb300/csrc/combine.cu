@@ -1,0 +1,121 @@
+// Split-KV combine and the standalone state merge.
+//
+// When the planner splits a row group's KV range into n parts, each part k
+// leaves (O_k normalised by its own sum, LSE_k natural log).  The exact
+// unsplit result is, with M = max_k LSE_k and w_k = exp(LSE_k - M),
+//   O = sum_k w_k O_k / sum_k w_k,   LSE = M + ln sum_k w_k.
+// Parts with LSE = -inf (no visible key) carry weight 0.  Not on the pages:
+// this is the identity that makes split-KV equal to unsplit attention.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mcp_internal.h"
+#include "ptx.cuh"
+
+namespace mcp {
+namespace {
+
+constexpr float kLog2e = 1.44269504088896341f;
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// One CTA per combine entry, one warp per row; lane l holds D/32 columns.
+template <int D>
+__global__ void __launch_bounds__(128) combine_kernel(const CombineEntry* __restrict__ ents,
+                                                      const int32_t* __restrict__ cu_q,
+                                                      const float* __restrict__ part_o,
+                                                      const float* __restrict__ part_lse,
+                                                      __nv_bfloat16* __restrict__ out,
+                                                      float* __restrict__ lse, int hq, int G) {
+  constexpr int V = D / 32;
+  const CombineEntry e = ents[blockIdx.x];
+  const int q_start = cu_q[e.seg];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int row = warp; row < e.rows; row += blockDim.x / 32) {
+    float M = neg_inf();
+    for (int k = 0; k < e.num_splits; ++k)
+      M = fmaxf(M, part_lse[e.part_row + static_cast<int64_t>(k) * e.rows + row]);
+    float acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    float L = 0.f;
+    for (int k = 0; k < e.num_splits; ++k) {
+      const int64_t pr = e.part_row + static_cast<int64_t>(k) * e.rows + row;
+      const float lk = part_lse[pr];
+      const float w = (lk == neg_inf()) ? 0.f : ptx::ex2((lk - M) * kLog2e);
+      L += w;
+      const float* src = part_o + pr * D + lane * V;
+#pragma unroll
+      for (int v = 0; v < V; ++v) acc[v] += w * src[v];
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int tok = e.q_begin + row / G;
+    const int g = row - (row / G) * G;
+    const int64_t orow = static_cast<int64_t>(q_start + tok) * hq + e.kv_head * G + g;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out + orow * D + lane * V);
+#pragma unroll
+    for (int v = 0; v < V; v += 2) dst[v / 2] = ptx::pack_bf16x2(acc[v] * inv, acc[v + 1] * inv);
+    if (lse && lane == 0) lse[orow] = L > 0.f ? M + logf(L) : neg_inf();
+  }
+}
+
+// Standalone merge: one warp per (row, head); o_parts [n, rows, heads, D].
+__global__ void __launch_bounds__(128) merge_states_kernel(const float* __restrict__ o_parts,
+                                                           const float* __restrict__ lse_parts,
+                                                           int n, int rows, int heads, int D,
+                                                           __nv_bfloat16* __restrict__ out,
+                                                           float* __restrict__ lse_out) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int64_t rh = static_cast<int64_t>(rows) * heads;
+  if (idx >= rh) return;
+  float M = neg_inf();
+  for (int k = 0; k < n; ++k) M = fmaxf(M, lse_parts[k * rh + idx]);
+  float L = 0.f;
+  for (int k = 0; k < n; ++k) {
+    const float lk = lse_parts[k * rh + idx];
+    L += (lk == neg_inf()) ? 0.f : ptx::ex2((lk - M) * kLog2e);
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  for (int d = lane; d < D; d += 32) {
+    float a = 0.f;
+    for (int k = 0; k < n; ++k) {
+      const float lk = lse_parts[k * rh + idx];
+      if (lk == neg_inf()) continue;
+      a += ptx::ex2((lk - M) * kLog2e) * o_parts[(k * rh + idx) * D + d];
+    }
+    out[idx * D + d] = __float2bfloat16_rn(a * inv);
+  }
+  if (lse_out && lane == 0) lse_out[idx] = L > 0.f ? M + logf(L) : neg_inf();
+}
+
+}  // namespace
+
+int launch_combine(const FwdArgs& a, void* stream) {
+  if (a.num_combine <= 0) return 0;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (a.head_dim == 128) {
+    combine_kernel<128><<<a.num_combine, 128, 0, st>>>(
+        a.combine, a.cu_seqlens_q, a.part_o, a.part_lse, static_cast<__nv_bfloat16*>(a.out), a.lse,
+        a.num_q_heads, G);
+  } else {
+    combine_kernel<64><<<a.num_combine, 128, 0, st>>>(
+        a.combine, a.cu_seqlens_q, a.part_o, a.part_lse, static_cast<__nv_bfloat16*>(a.out), a.lse,
+        a.num_q_heads, G);
+  }
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_merge_states(const float* o_parts, const float* lse_parts, int32_t n, int32_t rows,
+                        int32_t heads, int32_t head_dim, void* out, float* lse_out, void* stream) {
+  const int64_t rh = static_cast<int64_t>(rows) * heads;
+  if (rh == 0) return 0;
+  const int64_t blocks = (rh + 3) / 4;
+  merge_states_kernel<<<static_cast<int>(blocks), 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      o_parts, lse_parts, n, rows, heads, head_dim, static_cast<__nv_bfloat16*>(out), lse_out);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace mcp

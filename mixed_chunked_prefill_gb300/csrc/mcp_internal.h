@@ -1,0 +1,83 @@
+// Internal definitions shared by the host planner (host.cpp) and the CUDA
+// kernels (*.cu).  Plain C++ data; no CUDA types.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mcp {
+
+enum ItemKind : int32_t { kDecodeItem = 0, kPrefillItem = 1 };
+
+constexpr int kDecodeMaxRows = 16;   // query rows of a decode item: one m16 MMA tile
+constexpr int kTileRows = 128;       // query rows of a tensor-core tile (TMEM lanes)
+constexpr int kKvTile = 128;         // keys per tensor-core KV tile
+constexpr int kPageSize = 16;        // tokens per KV page supported by the kernels
+constexpr int kFwdThreads = 192;     // 6 warps: TMA producer, MMA issuer, 4 compute
+
+// One unit of work of the fused kernel (one CTA).  32 bytes.
+struct WorkItem {
+  int32_t seg;       // segment index in the stream
+  int32_t kv_head;   // kv head; the item covers its G query heads
+  int32_t kind;      // ItemKind
+  int32_t q_begin;   // first query token of the item, counted inside the segment
+  int32_t q_count;   // query tokens covered
+  int32_t kv_begin;  // first key position (multiple of 16, or of 128 for prefill)
+  int32_t kv_end;    // one past the last key position the item reads
+  int32_t part_row;  // -1: write out/lse directly; else first row in the partial buffers
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+
+// A row group whose KV range was split: its num_splits partial results sit at
+// rows part_row + k * rows (k < num_splits) of the partial buffers.  32 bytes.
+struct CombineEntry {
+  int32_t seg;
+  int32_t kv_head;
+  int32_t q_begin;
+  int32_t q_count;
+  int32_t num_splits;
+  int32_t part_row;
+  int32_t rows;      // q_count * G
+  int32_t pad;
+};
+static_assert(sizeof(CombineEntry) == 32, "CombineEntry layout");
+
+struct FwdArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqlens_k;
+  void* out;
+  float* lse;
+  const WorkItem* items;
+  const CombineEntry* combine;
+  float* part_o;
+  float* part_lse;
+  int32_t* error_word;
+  int32_t num_items;
+  int32_t num_combine;
+  int32_t total_q;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int32_t max_pages_per_seq;
+  int32_t num_pages;
+  float sm_scale;
+};
+
+// Launchers (return a cudaError_t value; 0 = success).  Defined in *.cu.
+int launch_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                  int32_t num_tokens, int32_t row_bytes, int64_t num_slots, void* k_cache,
+                  void* v_cache, int32_t* error_word, void* stream);
+int launch_mixed_attn(const FwdArgs& a, void* stream);
+int launch_combine(const FwdArgs& a, void* stream);
+int launch_merge_states(const float* o_parts, const float* lse_parts, int32_t n, int32_t rows,
+                        int32_t heads, int32_t head_dim, void* out, float* lse_out, void* stream);
+// Message of the last launcher failure that was not a CUDA error (e.g. a tensor
+// map the driver rejected), "" otherwise.
+const char* launch_detail();
+
+}  // namespace mcp

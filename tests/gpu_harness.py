@@ -1,0 +1,100 @@
+"""GPU-side test glue: runs the CUDA library on a synthetic workload and the
+oracle on the same inputs.  Test infrastructure only."""
+
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+from harness import OracleStep, rel_rms
+
+ATOL = 2e-2       # max |err| on bf16 outputs
+RMS_TOL = 1e-2    # relative RMS on bf16 outputs
+LSE_TOL = 1e-2    # max |err| on the natural-log LSE
+
+
+def gpu_step(w, t, options=None, fill=float("nan"), device="cuda", want_lse=True):
+    """Run append + fused attention for workload ``w`` with tensors ``t`` (on
+    any device); returns (out, lse, k_cache, v_cache, step) on the device."""
+    import torch
+
+    from mixed_chunked_prefill_gb300.step import MixedStep, write_history
+
+    td = {k: v.to(device) for k, v in t.items()}
+    shape = (w.num_pages, w.page_size, w.num_kv_heads, w.head_dim)
+    k_cache = torch.full(shape, fill, dtype=torch.bfloat16, device=device)
+    v_cache = torch.full(shape, fill, dtype=torch.bfloat16, device=device)
+    bt = w.block_tables()
+    write_history(bt, w.hist_lens, td["k_hist"], td["v_hist"], k_cache, v_cache, w.page_size)
+    cu = np.concatenate([[0], np.cumsum(w.q_lens)]).astype(np.int32)
+    step = MixedStep(w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size, w.num_pages,
+                     w.sm_scale, cu, w.k_lens, bt, device=device, options=options)
+    out = torch.full_like(td["q"], float("nan"))
+    lse = (torch.full((w.total_q, w.num_q_heads), float("nan"), dtype=torch.float32, device=device)
+           if want_lse else None)
+    step.run(td["q"], td["k_new"], td["v_new"], k_cache, v_cache, out, lse)
+    step.check()
+    torch.cuda.synchronize()
+    return out, lse, k_cache, v_cache, step
+
+
+def compare(w, out, lse, ref_out, ref_lse, rows=None, label=""):
+    """Element-wise check of GPU outputs against the oracle."""
+    got = out.float().cpu().numpy()
+    if rows is not None:
+        got, ref_out = got[rows], ref_out[rows]
+    assert np.isfinite(got).all(), f"{label}: non-finite output"
+    err = float(np.abs(got - ref_out).max()) if got.size else 0.0
+    rr = rel_rms(got, ref_out) if got.size else 0.0
+    assert err <= ATOL, f"{label}: max|err| {err:.4g} > {ATOL}"
+    assert rr <= RMS_TOL, f"{label}: rel RMS {rr:.4g} > {RMS_TOL}"
+    lerr = 0.0
+    if lse is not None:
+        gl = lse.cpu().numpy()
+        rl = ref_lse
+        if rows is not None:
+            gl, rl = gl[rows], rl[rows]
+        lerr = float(np.abs(gl - rl).max()) if gl.size else 0.0
+        assert lerr <= LSE_TOL, f"{label}: lse max|err| {lerr:.4g}"
+    return err, rr, lerr
+
+
+def per_segment_rel_rms(w, out, ref_out):
+    got = out.float().cpu().numpy()
+    cu = np.concatenate([[0], np.cumsum(w.q_lens)])
+    res = []
+    for s in range(w.num_seqs):
+        if w.q_lens[s]:
+            res.append(rel_rms(got[cu[s]:cu[s + 1]], ref_out[cu[s]:cu[s + 1]]))
+    return res
+
+
+def sub_workload(w, t, segs):
+    """The segments ``segs`` of ``w`` as their own workload (same lengths, same
+    physical pages), with their slices of the tensors on the CPU -- so the oracle
+    can check a few rows of a workload too large to run whole."""
+    import torch
+
+    cu = np.concatenate([[0], np.cumsum(w.q_lens)])
+    hcu = np.concatenate([[0], np.cumsum(w.hist_lens)])
+    sub = synth.Workload(w.name + "-sub", w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
+                         w.sm_scale, [w.q_lens[s] for s in segs], [w.k_lens[s] for s in segs],
+                         w.seed)
+    bt_full = w.block_tables()
+    sub.page_perm = w.page_perm
+    rows_bt = np.full((len(segs), sub.max_pages_per_seq), -1, dtype=np.int32)
+    for i, s in enumerate(segs):
+        n = w.pages_of(s)
+        rows_bt[i, :n] = bt_full[s, :n]
+    sub.block_tables = lambda: rows_bt  # same physical pages as in the full workload
+    ts = {}
+    for name in ("q", "k_new", "v_new"):
+        ts[name] = torch.cat([t[name][cu[s]:cu[s + 1]] for s in segs]).cpu()
+    for name in ("k_hist", "v_hist"):
+        ts[name] = torch.cat([t[name][hcu[s]:hcu[s + 1]] for s in segs]).cpu()
+    return sub, ts
+
+
+__all__ = ["gpu_step", "compare", "per_segment_rel_rms", "sub_workload", "OracleStep", "oracle",
+           "ATOL", "RMS_TOL", "LSE_TOL"]

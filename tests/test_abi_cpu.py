@@ -1,0 +1,317 @@
+"""C ABI checks that need no GPU: the library loads and exports every symbol
+include/mcp.h declares; host-side validation; the slot-mapping builder against
+the oracle (bit-exact); the work planner's coverage invariants."""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import mixed_chunked_prefill_gb300 as mcp
+import oracle
+import synth
+from mixed_chunked_prefill_gb300 import _capi
+from plan_tools import desc_for, plan_host
+
+ROOT = Path(__file__).resolve().parent.parent
+HEADER = ROOT / "include" / "mcp.h"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    from mixed_chunked_prefill_gb300 import build
+
+    build.build()
+    return mcp.load()
+
+
+def header_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mcp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = mcp.load()
+    names = header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in mcp.h but not exported"
+    assert set(names) == set(_capi.SIGNATURES), "binding signatures out of sync with mcp.h"
+
+
+def test_status_strings_and_version():
+    lib = mcp.load()
+    for code, name in [(0, b"MCP_OK"), (1, b"MCP_ERR_INVALID_ARG"), (2, b"MCP_ERR_UNSUPPORTED"),
+                       (3, b"MCP_ERR_WORKSPACE_TOO_SMALL"), (4, b"MCP_ERR_CUDA"),
+                       (5, b"MCP_ERR_TIMEOUT"), (6, b"MCP_ERR_DEVICE_CHECK")]:
+        assert lib.mcp_status_string(code) == name
+    assert lib.mcp_status_string(99) == b"MCP_ERR_UNKNOWN"
+    assert mcp.abi_version() == 1
+
+
+# ---------------------------------------------------------------------------
+# validation (returns before touching the device)
+# ---------------------------------------------------------------------------
+
+def _plan_status(desc, cu, sk, **kw):
+    st, *_ = plan_host(desc, cu, sk, **kw)
+    return st
+
+
+def base_desc(**over):
+    d = dict(num_seqs=3, total_q=1810, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+             max_pages_per_seq=625, num_pages=700, sm_scale=1 / math.sqrt(128))
+    d.update(over)
+    return mcp.make_desc(**d)
+
+
+CU = [0, 1, 2, 1810]
+SK = [121, 46, 10000]
+
+
+def test_valid_worked_layout_plans():
+    assert _plan_status(base_desc(), CU, SK) == _capi.MCP_OK
+
+
+@pytest.mark.parametrize("over,cu,sk,code", [
+    (dict(num_q_heads=30), CU, SK, _capi.MCP_ERR_INVALID_ARG),          # H_q % H_kv
+    (dict(head_dim=96), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
+    (dict(page_size=32), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
+    (dict(num_pages=0), CU, SK, _capi.MCP_ERR_INVALID_ARG),
+    (dict(max_pages_per_seq=100), CU, SK, _capi.MCP_ERR_INVALID_ARG),   # 10000 keys need 625 pages
+    (dict(total_q=1811), CU, SK, _capi.MCP_ERR_INVALID_ARG),
+    (dict(), [1, 1, 2, 1810], SK, _capi.MCP_ERR_INVALID_ARG),           # cu[0] != 0
+    (dict(), [0, 2, 1, 1810], SK, _capi.MCP_ERR_INVALID_ARG),           # decreasing
+    (dict(), CU, [121, 0, 10000], _capi.MCP_ERR_INVALID_ARG),           # Lq > Lk
+    (dict(), CU, [121, 46, 1000], _capi.MCP_ERR_INVALID_ARG),           # chunk longer than its KV
+    (dict(), CU, [121, -1, 10000], _capi.MCP_ERR_INVALID_ARG),
+    (dict(sm_scale=float("nan")), CU, SK, _capi.MCP_ERR_INVALID_ARG),
+    (dict(num_q_heads=1024, num_kv_heads=4), CU, SK, _capi.MCP_ERR_UNSUPPORTED),  # group > 128
+])
+def test_plan_rejects_bad_metadata(over, cu, sk, code):
+    assert _plan_status(base_desc(**over), cu, sk) == code
+    assert mcp.load().mcp_last_error() != b""
+
+
+def test_plan_rejects_null_and_reserved_options():
+    lib = mcp.load()
+    cu = np.array(CU, dtype=np.int32)
+    plan = mcp.Plan()
+    d = base_desc()
+    assert lib.mcp_mixed_attn_plan_host(None, cu.ctypes.data_as(ctypes.c_void_p), None, None,
+                                        ctypes.byref(plan), None, 0) == _capi.MCP_ERR_INVALID_ARG
+    assert lib.mcp_mixed_attn_plan_host(ctypes.byref(d), None, None, None, ctypes.byref(plan),
+                                        None, 0) == _capi.MCP_ERR_INVALID_ARG
+    opts = mcp.PlanOptions(152, 0, 0)
+    opts.reserved[1] = 3
+    sk = np.array(SK, dtype=np.int32)
+    assert lib.mcp_mixed_attn_plan_host(ctypes.byref(d), cu.ctypes.data_as(ctypes.c_void_p),
+                                        sk.ctypes.data_as(ctypes.c_void_p), ctypes.byref(opts),
+                                        ctypes.byref(plan), None, 0) == _capi.MCP_ERR_INVALID_ARG
+
+
+def test_plan_host_buffer_too_small():
+    lib = mcp.load()
+    st, plan, _, _ = plan_host(base_desc(), CU, SK)
+    assert st == 0
+    cu = np.array(CU, dtype=np.int32)
+    sk = np.array(SK, dtype=np.int32)
+    buf = np.zeros(16, dtype=np.uint8)
+    opts = mcp.PlanOptions(152, 0, 0)
+    assert lib.mcp_mixed_attn_plan_host(
+        ctypes.byref(base_desc()), cu.ctypes.data_as(ctypes.c_void_p),
+        sk.ctypes.data_as(ctypes.c_void_p), ctypes.byref(opts), ctypes.byref(plan),
+        buf.ctypes.data_as(ctypes.c_void_p), buf.size) == _capi.MCP_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_append_validation_before_launch():
+    lib = mcp.load()
+    assert lib.mcp_paged_kv_append(None, None, None, -1, 8, 128, 16, 10, None, None, None,
+                                   None) == _capi.MCP_ERR_INVALID_ARG
+    assert lib.mcp_paged_kv_append(None, None, None, 4, 8, 128, 16, 10, None, None, None,
+                                   None) == _capi.MCP_ERR_INVALID_ARG
+    assert lib.mcp_paged_kv_append(None, None, None, 4, 3, 5, 16, 10, None, None, None,
+                                   None) == _capi.MCP_ERR_INVALID_ARG   # row not 16-byte multiple
+    assert lib.mcp_paged_kv_append(None, None, None, 0, 8, 128, 16, 10, None, None, None,
+                                   None) == _capi.MCP_OK               # nothing to do
+
+
+def test_fwd_validation_before_launch():
+    lib = mcp.load()
+    bogus = mcp.Plan()
+    assert lib.mcp_mixed_attn_fwd(ctypes.byref(bogus), *([None] * 9), 0, None) == \
+        _capi.MCP_ERR_INVALID_ARG
+    st, plan, _, _ = plan_host(base_desc(), CU, SK)
+    assert lib.mcp_mixed_attn_fwd(ctypes.byref(plan), *([None] * 9), 0, None) == \
+        _capi.MCP_ERR_INVALID_ARG
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check fails first
+    assert lib.mcp_mixed_attn_fwd(ctypes.byref(plan), fake, fake, fake, fake, fake, fake, fake,
+                                  None, fake, 16, None) == _capi.MCP_ERR_WORKSPACE_TOO_SMALL
+    assert lib.mcp_merge_states(None, None, 0, 1, 1, 8, None, None, None) == \
+        _capi.MCP_ERR_INVALID_ARG
+    assert lib.mcp_check_device_errors(None, None) == _capi.MCP_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------------------
+# slot mapping: the C builder equals the oracle, bit for bit
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", synth.CONFIG_NAMES)
+def test_slot_mapping_matches_oracle(name):
+    w = synth.make_workload(name)
+    bt = w.block_tables()
+    cu, _, _, _ = oracle.segment_layout(w.q_lens, w.k_lens)
+    table = oracle.page_table_from_block_tables(bt, w.k_lens, w.page_size)
+    expect = oracle.new_token_slots(table, cu, w.k_lens)
+    got = mcp.build_slot_mapping(bt, cu, w.k_lens, w.page_size, w.num_pages)
+    assert got.dtype == np.int64
+    assert np.array_equal(got, expect)
+
+
+def test_slot_mapping_history_layout_matches_oracle():
+    # the same builder fills history positions (a step whose tokens are the history)
+    w = synth.make_workload("balanced")
+    bt = w.block_tables()
+    hist = w.hist_lens
+    cu_h, _, _, _ = oracle.segment_layout(hist, hist)
+    table = oracle.page_table_from_block_tables(bt, w.k_lens, w.page_size)
+    expect = oracle.new_token_slots(table, cu_h, hist)
+    got = mcp.build_slot_mapping(bt, cu_h, hist, w.page_size, w.num_pages)
+    assert np.array_equal(got, expect)
+
+
+def test_slot_mapping_rejects_page_outside_pool():
+    bt = np.array([[0, 1, 99]], dtype=np.int32)
+    with pytest.raises(mcp.MCPError):
+        mcp.build_slot_mapping(bt, [0, 3], [40], 16, 10)
+
+
+# ---------------------------------------------------------------------------
+# planner invariants
+# ---------------------------------------------------------------------------
+
+def check_plan_covers(w, items, comb, plan):
+    """Every (segment, kv head, query token) row is covered by exactly one set
+    of items whose KV ranges tile [0, visible end of the item's last token)."""
+    G = w.num_q_heads // w.num_kv_heads
+    cu, _, _, _ = oracle.segment_layout(w.q_lens, w.k_lens)
+    assert plan.num_items == len(items)
+    assert plan.num_decode_items + plan.num_prefill_items == len(items)
+    cover = {}
+    for it in items:
+        s, h = int(it["seg"]), int(it["kv_head"])
+        lq, lk = w.q_lens[s], w.k_lens[s]
+        assert 0 <= it["q_begin"] and it["q_begin"] + it["q_count"] <= lq and it["q_count"] > 0
+        assert 0 <= it["kv_begin"] < it["kv_end"] <= lk
+        vis_end = lk - lq + it["q_begin"] + it["q_count"]
+        assert it["kv_end"] <= vis_end
+        if it["kind"] == 0:
+            assert it["q_count"] * G <= 16 and it["kv_begin"] % 16 == 0
+            assert it["q_begin"] == 0 and it["q_count"] == lq
+        else:
+            assert it["q_count"] * G <= 128 and it["kv_begin"] % 128 == 0
+            assert it["q_count"] * G > 16 or lq * G > 16
+        key = (s, h, int(it["q_begin"]), int(it["q_count"]))
+        cover.setdefault(key, []).append((int(it["kv_begin"]), int(it["kv_end"]), int(it["part_row"])))
+    # each row group: KV ranges tile [0, vis_end)
+    rows_seen = {}
+    for (s, h, qb, qc), ranges in cover.items():
+        ranges.sort()
+        vis_end = w.k_lens[s] - w.q_lens[s] + qb + qc
+        assert ranges[0][0] == 0 and ranges[-1][1] == vis_end
+        for a, b in zip(ranges[:-1], ranges[1:]):
+            assert a[1] == b[0]
+        if len(ranges) == 1:
+            assert ranges[0][2] == -1
+        else:
+            assert all(r[2] >= 0 for r in ranges)
+        for t in range(qb, qb + qc):
+            rows_seen[(s, h, t)] = rows_seen.get((s, h, t), 0) + 1
+    for s in range(w.num_seqs):
+        for h in range(w.num_kv_heads):
+            for t in range(w.q_lens[s]):
+                assert rows_seen.get((s, h, t), 0) == 1, (s, h, t)
+    # combine entries match the split groups; partial rows never overlap
+    split_groups = {k: v for k, v in cover.items() if len(v) > 1}
+    assert len(comb) == len(split_groups) == plan.num_combine
+    used = np.zeros(int(plan.partial_rows), dtype=np.int32)
+    for e in comb:
+        key = (int(e["seg"]), int(e["kv_head"]), int(e["q_begin"]), int(e["q_count"]))
+        ranges = split_groups[key]
+        assert e["num_splits"] == len(ranges) and e["rows"] == e["q_count"] * G
+        parts = sorted(r[2] for r in ranges)
+        assert parts == [int(e["part_row"]) + k * int(e["rows"]) for k in range(len(ranges))]
+        used[e["part_row"]:e["part_row"] + e["num_splits"] * e["rows"]] += 1
+    assert (used <= 1).all()
+
+
+@pytest.mark.parametrize("name", synth.CONFIG_NAMES)
+def test_planner_covers_every_row_once(name):
+    w = synth.make_workload(name)
+    cu, _, _, _ = oracle.segment_layout(w.q_lens, w.k_lens)
+    st, plan, items, comb = plan_host(desc_for(w), cu, w.k_lens)
+    assert st == 0
+    check_plan_covers(w, items, comb, plan)
+
+
+@pytest.mark.parametrize("dsplit,psplit", [(16, 128), (48, 256), (1024, 1024)])
+def test_planner_forced_splits(dsplit, psplit):
+    for name in ("tiny", "worked"):
+        w = synth.make_workload(name)
+        cu, _, _, _ = oracle.segment_layout(w.q_lens, w.k_lens)
+        st, plan, items, comb = plan_host(desc_for(w), cu, w.k_lens, dsplit=dsplit, psplit=psplit)
+        assert st == 0
+        assert plan.decode_split_tokens == -(-dsplit // 16) * 16
+        assert plan.prefill_split_tokens == -(-psplit // 128) * 128
+        check_plan_covers(w, items, comb, plan)
+        if psplit < 10000 or dsplit < 121:
+            assert plan.num_combine > 0 or name == "tiny"
+
+
+def test_planner_random_shapes():
+    rng = np.random.Generator(np.random.PCG64(123))
+    for trial in range(40):
+        hkv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 3, 4, 8, 16]))
+        S = int(rng.integers(1, 9))
+        q, k = [], []
+        for _ in range(S):
+            lq = int(rng.choice([0, 1, 1, 2, 3, 17, 100, 300]))
+            hist = int(rng.integers(0, 3000))
+            q.append(lq)
+            k.append(max(lq + hist, 1 if lq > 0 else 0))
+        w = synth.make_workload_from_lengths("r", G * hkv, hkv, 128, 16, 0.1, q, k, 7 + trial)
+        cu, _, _, _ = oracle.segment_layout(q, k)
+        st, plan, items, comb = plan_host(desc_for(w), cu, k, num_sms=int(rng.integers(1, 200)),
+                                          dsplit=int(rng.choice([0, 64, 512])),
+                                          psplit=int(rng.choice([0, 256, 1024])))
+        assert st == 0
+        check_plan_covers(w, items, comb, plan)
+
+
+def test_planner_balance_bound_big_configs():
+    # greedy list scheduling of the planned order over 152 SMs stays close to the
+    # lower bound max(total / SMs, longest item) under the planner's own cost units
+    for name in ("decode-heavy", "long-context"):
+        w = synth.make_workload(name)
+        cu, _, _, _ = oracle.segment_layout(w.q_lens, w.k_lens)
+        st, plan, items, comb = plan_host(desc_for(w), cu, w.k_lens)
+        D = w.head_dim
+        cost = np.where(items["kind"] == 0, (items["kv_end"] - items["kv_begin"]) * 4.0 * D / 45.0,
+                        300.0 + np.ceil((items["kv_end"] - items["kv_begin"]) / 128)
+                        * 4.0 * 128 * 128 * D / 6000.0)
+        import heapq
+        sms = [0.0] * 152
+        heapq.heapify(sms)
+        for c in cost:
+            t = heapq.heappop(sms)
+            heapq.heappush(sms, t + c)
+        makespan = max(sms)
+        lower = max(cost.sum() / 152, cost.max())
+        assert makespan <= 1.1 * lower, (name, makespan / lower)
