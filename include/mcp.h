@@ -265,6 +265,40 @@ mcp_status mcp_merge_states(const float* o_parts, const float* lse_parts, int32_
                             int32_t heads, int32_t head_dim, void* out, float* lse_out,
                             void* stream);
 
+/* ------------------------------------------------------------------------- */
+/* mixed attention forward without a workspace                              */
+/* ------------------------------------------------------------------------- */
+/*
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory when they run a step (e.g. inside a framework
+ * whose memory pool owns every device allocation, or a server that must not
+ * grow its device footprint after start-up).  It plans the step on the host
+ * exactly like mcp_mixed_attn_plan and runs mcp_mixed_attn_fwd, but keeps the
+ * work lists, split partials and error word in a fixed 16 MiB device array
+ * owned by the library instead of a caller workspace.  It allocates no device
+ * memory (the planner's host-side working lists use ordinary host memory).
+ *
+ * Inputs and outputs are those of mcp_mixed_attn_plan (host metadata, opts may
+ * be NULL) and mcp_mixed_attn_fwd (device tensors, stream).
+ * error_word: NULL, or receives the device address of the error word of this
+ *   call (valid until the next call; pass it to mcp_check_device_errors).
+ * Limits:
+ *  - a step whose plan needs more than 16 MiB of scratch returns
+ *    MCP_ERR_WORKSPACE_TOO_SMALL before anything is launched;
+ *  - every GPU that loads the library holds the 16 MiB array until exit;
+ *  - all calls share that array (it keeps the last call's contents; this call
+ *    clears what must start at zero), so calls whose GPU work overlaps -- on
+ *    different streams or from different threads -- race; order them;
+ *  - the first call on each device looks up the array's device address; make
+ *    that first call before any CUDA stream capture.
+ */
+mcp_status mcp_mixed_attn_fwd_noalloc(const mcp_attn_desc* desc, const int32_t* h_cu_seqlens_q,
+                                      const int32_t* h_seqlens_k, const mcp_plan_options* opts,
+                                      const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* cu_seqlens_q,
+                                      const int32_t* seqlens_k, void* out, float* lse,
+                                      int32_t** error_word, void* stream);
+
 /* Device-check bits written to an error word. */
 #define MCP_DEVERR_TIMEOUT 0x1      /* a bounded mbarrier wait gave up           */
 #define MCP_DEVERR_PAGE_RANGE 0x2   /* a block-table page id outside the pool    */

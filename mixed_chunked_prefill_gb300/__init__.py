@@ -27,7 +27,7 @@ from ._capi import (  # noqa: F401
 __all__ = [
     "AttnDesc", "Plan", "PlanOptions", "MCPError", "load", "abi_version", "paged_kv_append",
     "build_slot_mapping", "mixed_attn_plan", "mixed_attn_fwd", "check_device_errors",
-    "workspace_error_word", "merge_states", "make_desc",
+    "workspace_error_word", "merge_states", "make_desc", "mixed_attn_fwd_noalloc",
 ]
 
 
@@ -181,3 +181,28 @@ def merge_states(o_parts, lse_parts, out, lse_out=None, stream=None) -> None:
                               _dev(out, torch.bfloat16, "out"),
                               _dev(lse_out, torch.float32, "lse_out"), _stream(stream))
     _capi.check(st, "merge_states")
+
+
+def mixed_attn_fwd_noalloc(desc: AttnDesc, h_cu_seqlens_q, h_seqlens_k, q, k_cache, v_cache,
+                           block_tables, cu_seqlens_q, seqlens_k, out, lse=None,
+                           options: PlanOptions | None = None, stream=None) -> int:
+    """Mixed attention forward without a workspace (for callers that cannot
+    allocate device memory): plans from the HOST metadata and keeps its scratch
+    in the library's fixed 16 MiB device array.  Returns the device address of
+    this call's error word (for check_device_errors).  Calls that overlap on
+    the GPU race; make the first call on a device before any stream capture."""
+    import torch
+
+    lib = load()
+    cu, cu_p = _host_i32(h_cu_seqlens_q, "h_cu_seqlens_q")
+    sk, sk_p = _host_i32(h_seqlens_k, "h_seqlens_k")
+    ew = ctypes.c_void_p()
+    st = lib.mcp_mixed_attn_fwd_noalloc(
+        ctypes.byref(desc), cu_p, sk_p, ctypes.byref(options) if options is not None else None,
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),
+        _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _dev(seqlens_k, torch.int32, "seqlens_k"),
+        _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse"), ctypes.byref(ew),
+        _stream(stream))
+    _capi.check(st, "mixed_attn_fwd_noalloc")
+    return int(ew.value or 0)

@@ -286,6 +286,13 @@ thread_local std::vector<unsigned char> g_staging;
 
 }  // namespace
 
+namespace mcp {
+int32_t set_error_code(int32_t status, const char* msg) {
+  snprintf(g_err, sizeof(g_err), "%s", msg ? msg : "");
+  return status;
+}
+}  // namespace mcp
+
 extern "C" {
 
 const char* mcp_status_string(int32_t s) {

@@ -76,6 +76,9 @@ int launch_mixed_attn(const FwdArgs& a, void* stream);
 int launch_combine(const FwdArgs& a, void* stream);
 int launch_merge_states(const float* o_parts, const float* lse_parts, int32_t n, int32_t rows,
                         int32_t heads, int32_t head_dim, void* out, float* lse_out, void* stream);
+// Record `msg` as this thread's mcp_last_error() and return `status`.
+// Defined in host.cpp.
+int32_t set_error_code(int32_t status, const char* msg);
 // Message of the last launcher failure that was not a CUDA error (e.g. a tensor
 // map the driver rejected), "" otherwise.
 const char* launch_detail();
