@@ -131,7 +131,7 @@ typedef struct mcp_attn_desc {
   int32_t page_size;         /* P: 16                                            */
   int32_t max_pages_per_seq; /* row length of block_tables                       */
   int32_t num_pages;         /* pages in each cache tensor                       */
-  float sm_scale;            /* score scale, e.g. 1/sqrt(D) ([K] kernel launch)  */
+  float sm_scale;            /* score scale > 0, e.g. 1/sqrt(D) ([K] kernel launch) */
 } mcp_attn_desc;
 
 typedef struct mcp_plan_options {
@@ -198,12 +198,13 @@ mcp_status mcp_mixed_attn_plan(const mcp_attn_desc* desc, const int32_t* h_cu_se
  * start of its device workspace and zeroes the 4-byte error word at
  * plan->off_error gets the same state mcp_mixed_attn_plan uploads.
  * host_buffer == NULL: sizing only.  Host only; needs no GPU when
- * opts->num_sms > 0.  Item layout (32 bytes, int32 fields): segment, kv head,
- * kind (0 decode, 1 tensor-core tile), first query token inside the segment,
- * query token count, first key, one past the last key, partial row (-1 =
- * written directly).  Combine entry (32 bytes, int32): segment, kv head, first
- * query token, query token count, number of splits, first partial row, rows
- * per split, 0.
+ * opts->num_sms > 0.  Item layout (32 bytes, little-endian): int32 segment,
+ * int16 first kv head, int8 kind (0 decode, 1 tensor-core tile), int8 number of
+ * kv heads covered, int32 first query token inside the segment, int32 query
+ * token count, int32 first key, int32 one past the last key, int32 partial row
+ * of the first head (-1 = written directly), int32 partial rows between heads.
+ * Combine entry (32 bytes, int32): segment, kv head, first query token, query
+ * token count, number of splits, first partial row, rows per split, 0.
  */
 mcp_status mcp_mixed_attn_plan_host(const mcp_attn_desc* desc, const int32_t* h_cu_seqlens_q,
                                     const int32_t* h_seqlens_k, const mcp_plan_options* opts,

@@ -3,19 +3,25 @@
 // One launch serves the whole packed token stream ([K] "平铺策略 / 掩码特化":
 // one kernel for prefill chunks and decodes; [W] "Flash Attention 的 varlen
 // 接口": the i-th query segment attends only to the i-th KV segment,
-// right-aligned causal).  Each CTA runs one work item from the host plan:
+// right-aligned causal).  Each CTA (10 warps) runs one work item of the host
+// plan:
 //
-//  * prefill item -- 128 query rows (the G query heads of one kv head packed
-//    with 128/G tokens) against a KV range in 128-key tiles.  Warp 0 issues TMA
-//    page loads (8 pages x 16 tokens per tile, each page through the block
-//    table), warp 1 issues tcgen05.mma (S = Q K^T into TMEM, O += P V into
-//    TMEM), warps 2-5 run the online softmax on S rows read from TMEM, write P
-//    (bf16) to shared memory and rescale O lazily.  Only tiles that straddle
-//    the diagonal are masked ([K] "掩码特化").
-//  * decode item -- the G*Lq (<= 16) query rows of one kv head against a KV
-//    range, page by page: warp 0 streams K/V pages with TMA into a 16-stage
-//    ring, warps 2-5 each take every 4th page (ldmatrix + mma.sync m16n8k16,
-//    quad-shuffle max/sum, online softmax) and merge their states at the end.
+//  * tensor-core item -- 128 query rows (the G query heads of one kv head
+//    packed with 128/G tokens) against a KV range in 128-key tiles.  Warp 0
+//    loads the Q tile with TMA; warps 6-9 load each K/V tile page by page
+//    through the block table (a tile is 8 pages x 2 panels x K,V = 32 TMA
+//    boxes, split over four warps because one warp issues boxes serially);
+//    warp 1 issues tcgen05.mma (S = Q K^T into TMEM, O += P V into TMEM);
+//    warps 2-5 run the online softmax on S rows read from TMEM, write P (bf16)
+//    to shared memory and rescale O lazily.  Only tiles that cross the
+//    diagonal are masked ([K] "掩码特化").
+//  * decode item -- the G*Lq (<= 16) query rows of each kv head of a head group
+//    (up to 8 heads) against a KV range.  Warp 0 streams whole pages for the
+//    group -- one TMA box per K page and one per V page, laid out in shared
+//    memory as [head][panel][token][64] -- through a multi-stage ring; warps 2-9
+//    each own one kv head (ldmatrix + mma.sync m16n8k16, quad-shuffle max/sum,
+//    online softmax); several warps share a head when the group is smaller
+//    than 8 and merge their states at the end.
 //
 // A split KV range writes (O, LSE) partials that combine.cu merges.
 //
@@ -41,49 +47,48 @@ constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per wait
 constexpr float kRescaleThreshold = 8.0f;  // rescale O only when the max grows by > 2^8
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
-constexpr int kDecStages = 16;  // decode page ring depth
+constexpr int kDecRingBytes = 192 * 1024;  // decode page ring
+constexpr int kMaxDecStages = 48;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
 template <int D>
 struct Cfg {
-  static constexpr int kHalves = D / 64;         // 64-column (128-byte) swizzle panels
-  static constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 B
-  // prefill
+  static constexpr int kHalves = D / 64;        // 64-column (128-byte) swizzle panels
+  static constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 B
+  // tensor-core item
   static constexpr int kQBytes = kHalves * kHalfBytes;
   static constexpr int kKvBytes = kHalves * kHalfBytes;  // one K (or V) tile of 128 keys
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kQBytes;                  // stage s: K at kOffK + 2*s*kKvBytes, V after
+  static constexpr int kOffK = kQBytes;  // stage s: K at kOffK + 2*s*kKvBytes, V after it
   static constexpr int kOffP = kOffK + 4 * kKvBytes;
-  static constexpr int kPBytes = 2 * kHalfBytes;         // P: 128 rows x 128 keys bf16
+  static constexpr int kPBytes = 2 * kHalfBytes;  // P: 128 rows x 128 keys bf16
   static constexpr int kPrefillBytes = kOffP + kPBytes;
-  // decode
-  static constexpr int kPageBytes = kHalves * kPageSize * 128;  // one page of one kv head
-  static constexpr int kStageBytes = 2 * kPageBytes;            // K page + V page
-  static constexpr int kOffRing = 0;
-  static constexpr int kOffMerge = kDecStages * kStageBytes;
-  static constexpr int kMergeBytes = 4 * 16 * D * 4 + 2 * 64 * 4;
-  static constexpr int kDecodeBytes = kOffMerge + kMergeBytes;
+  // decode item: ring of [K block | V block], block = [head][panel][16 tokens][128 B]
+  static constexpr int kHeadBlock = kHalves * kPageSize * 128;
+  static constexpr int kMergeBytes = 8 * 16 * D * 4 + 2 * 8 * 16 * 4;  // reuses the ring
+  static_assert(kMergeBytes <= kDecRingBytes, "merge area");
   // common
-  static constexpr int kDataBytes = kPrefillBytes > kDecodeBytes ? kPrefillBytes : kDecodeBytes;
+  static constexpr int kDataBytes = kPrefillBytes > kDecRingBytes ? kPrefillBytes : kDecRingBytes;
   static constexpr int kOffBar = (kDataBytes + 1023) & ~1023;
   static constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // barriers/flags + alignment slack
 };
 
 // barrier slots
 enum : int {
-  BQ = 0,       // Q tile landed
-  BK0 = 1,      // K tile of stage s landed (BK0 + s)
-  BV0 = 3,      // V tile of stage s landed
-  BE0 = 5,      // stage s free again (MMA done with K and V)
-  BS0 = 7,      // S buffer s holds Q K^T of the current tile
-  BP = 9,       // P of the current tile written (128 softmax threads)
-  BPV = 10,     // P V of the current tile accumulated into O
-  BDRAIN = 11,  // all MMAs of the CTA finished
-  BFULL0 = 16,  // decode ring stage landed
-  BEMPTY0 = 32, // decode ring stage free
-  kNumBars = 48
+  BQ = 0,        // Q tile landed
+  BK0 = 1,       // K tile of stage s landed (BK0 + s); two producer warps arrive
+  BV0 = 3,       // V tile of stage s landed; two producer warps arrive
+  BE0 = 5,       // stage s free again (MMA done with K and V)
+  BS0 = 7,       // S buffer s holds Q K^T of the current tile
+  BP = 9,        // P of the current tile written (128 softmax threads)
+  BPV = 10,      // P V of the current tile accumulated into O
+  BDRAIN = 11,   // all MMAs of the CTA finished
+  BFULL0 = 12,   // decode ring stage landed (12 .. 12+kMaxDecStages-1)
+  BEMPTY0 = BFULL0 + kMaxDecStages,  // decode ring stage free
+  kNumBars = BEMPTY0 + kMaxDecStages
 };
+static_assert(kNumBars * 8 + 32 <= 1024, "barrier block");
 
 struct Ctx {
   uint32_t bar;
@@ -92,32 +97,38 @@ struct Ctx {
   __device__ __forceinline__ uint32_t b(int i) const { return bar + 8u * static_cast<uint32_t>(i); }
 };
 
-// Wait for the phase with `parity` of barrier `bar` to complete; false if the
-// CTA aborted or the wait ran past kWaitLimitNs (then the CTA aborts).
-__device__ __noinline__ bool wait_on(const Ctx& c, uint32_t bar, uint32_t parity) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool wait_slow(volatile int* abort, int32_t* err, uint32_t bar,
+                                       uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer_ns();
 #pragma unroll 1
   while (true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*c.abort) return false;
+    if (*abort) return false;
     if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-      *c.abort = 1;
-      if (c.err) atomicOr(c.err, MCP_DEVERR_TIMEOUT);
+      *abort = 1;
+      if (err) atomicOr(err, MCP_DEVERR_TIMEOUT);
       return false;
     }
   }
 }
 
+// Wait for the phase with `parity` of barrier `bar` to complete; false if the
+// CTA aborted or the wait ran past kWaitLimitNs (then the CTA aborts).
+__device__ __forceinline__ bool wait_on(const Ctx& c, uint32_t bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_slow(c.abort, c.err, bar, parity);
+}
+
 // Bounded wait that ignores the abort flag: used to let this CTA's own async
 // copies / MMAs finish before it exits.
-__device__ __noinline__ void drain_wait(const Ctx& c, uint32_t bar, uint32_t parity) {
+__device__ __noinline__ void drain_wait(volatile int* abort, int32_t* err, uint32_t bar,
+                                        uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer_ns();
 #pragma unroll 1
   while (!ptx::mbar_try_wait(bar, parity)) {
     if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-      *c.abort = 1;
-      if (c.err) atomicOr(c.err, MCP_DEVERR_TIMEOUT);
+      *abort = 1;
+      if (err) atomicOr(err, MCP_DEVERR_TIMEOUT);
       return;
     }
   }
@@ -138,7 +149,8 @@ struct KParams {
   int32_t num_pages;
   int32_t hq;
   int32_t G;
-  float scale_log2;  // sm_scale * log2(e): scores live in log2 units
+  int32_t dec_stages;  // decode ring stages (a multiple of the warps sharing one head)
+  float scale_log2;    // sm_scale * log2(e): scores live in log2 units
 };
 
 struct Seg {
@@ -156,7 +168,7 @@ __device__ __forceinline__ int page_of(const KParams& p, int seg, int lp) {
 }
 
 // ------------------------------------------------------------------------
-// prefill item: tcgen05 tile
+// tensor-core item
 // ------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, const Seg& sg,
@@ -173,55 +185,55 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
   const uint32_t sP = base + C::kOffP;
   auto sK = [&](int s) { return base + C::kOffK + static_cast<uint32_t>(2 * s * C::kKvBytes); };
   auto sV = [&](int s) { return sK(s) + C::kKvBytes; };
+  constexpr int kPages = kKvTile / kPageSize;  // 8 pages per tile
 
   if (warp == 0) {
-    // ------------------------------------------------------ TMA producer
-    const uint64_t pol_q = ptx::policy_evict_first();
-    const uint64_t pol_kv = ptx::policy_evict_last();  // other q tiles re-read these K/V
+    // ------------------------------------------------------ Q tile (TMA)
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(c.b(BQ), C::kHalves * G * TQ * 128);
       for (int h = 0; h < C::kHalves; ++h)
         ptx::tma_load_4d(sQ + h * C::kHalfBytes, tm_q, c.b(BQ), 0, h, it.kv_head * G,
-                         sg.q_start + it.q_begin, pol_q);
+                         sg.q_start + it.q_begin, ptx::policy_evict_first());
     }
+    __syncwarp();
+    drain_wait(c.abort, c.err, c.b(BQ), 0);
+  } else if (warp >= 6) {
+    // -------------------------------------- K/V producers: four warps
+    // warp 6: K pages 0-3, warp 7: K pages 4-7, warp 8: V pages 0-3, warp 9: V pages 4-7
+    const int pr = warp - 6;
+    const bool isK = pr < 2;
+    const int pg0 = (pr & 1) * (kPages / 2);
+    const CUtensorMap* tm = isK ? tm_k : tm_v;
+    const uint64_t pol = ptx::policy_evict_last();  // other q tiles re-read these K/V
     int t = 0;
     for (; t < ntiles; ++t) {
       const int s = t & 1;
       if (t >= 2 && !wait_on(c, c.b(BE0 + s), ((t >> 1) + 1) & 1)) break;
       const int key0 = kv0 + t * kKvTile;
-      int npg = (kv1 - key0 + kPageSize - 1) / kPageSize;
-      npg = npg < kKvTile / kPageSize ? npg : kKvTile / kPageSize;
-      const int pg = lane < npg ? page_of(p, it.seg, key0 / kPageSize + lane) : p.num_pages;
-      int pgs[kKvTile / kPageSize];
+      int npg = (kv1 - key0 + kPageSize - 1) / kPageSize;  // pages of the tile inside the item
+      const int mine = lane < kPages / 2 && pg0 + lane < npg;
+      const int pg = mine ? page_of(p, it.seg, key0 / kPageSize + pg0 + lane) : p.num_pages;
+      int pgs[kPages / 2];
 #pragma unroll
-      for (int i = 0; i < kKvTile / kPageSize; ++i) pgs[i] = __shfl_sync(0xffffffffu, pg, i);
+      for (int i = 0; i < kPages / 2; ++i) pgs[i] = __shfl_sync(0xffffffffu, pg, i);
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(c.b(BK0 + s), C::kKvBytes);
+        const uint32_t bar = c.b((isK ? BK0 : BV0) + s);
+        const uint32_t dst = isK ? sK(s) : sV(s);
+        ptx::mbar_arrive_expect_tx(bar, C::kKvBytes / 2);
 #pragma unroll
-        for (int i = 0; i < kKvTile / kPageSize; ++i)
-#pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
-            ptx::tma_load_5d(sK(s) + h * C::kHalfBytes + i * kPageSize * 128, tm_k, c.b(BK0 + s),
-                             0, h, it.kv_head, 0, pgs[i], pol_kv);
-        ptx::mbar_arrive_expect_tx(c.b(BV0 + s), C::kKvBytes);
-#pragma unroll
-        for (int i = 0; i < kKvTile / kPageSize; ++i)
+        for (int i = 0; i < kPages / 2; ++i)
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h)
-            ptx::tma_load_5d(sV(s) + h * C::kHalfBytes + i * kPageSize * 128, tm_v, c.b(BV0 + s),
-                             0, h, it.kv_head, 0, pgs[i], pol_kv);
+            ptx::tma_load_5d(dst + h * C::kHalfBytes + (pg0 + i) * kPageSize * 128, tm, bar, 0, h,
+                             it.kv_head, 0, pgs[i], pol);
       }
       __syncwarp();
     }
-    // drain: the last tile issued into each stage, and Q
+    // drain: the last tile this warp issued into each stage
     for (int s = 0; s < 2; ++s) {
       const int last = (t - 1 - s) >= 0 ? (t - 1 - ((t - 1 - s) & 1)) : -1;
-      if (last >= 0) {
-        drain_wait(c, c.b(BK0 + s), (last >> 1) & 1);
-        drain_wait(c, c.b(BV0 + s), (last >> 1) & 1);
-      }
+      if (last >= 0) drain_wait(c.abort, c.err, c.b((isK ? BK0 : BV0) + s), (last >> 1) & 1);
     }
-    drain_wait(c, c.b(BQ), 0);
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     constexpr uint32_t kIdQK = ptx::idesc_bf16(128, kKvTile, false);
@@ -287,7 +299,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     if (issued) {
       if (lane == 0) ptx::mma_commit(c.b(BDRAIN));
       __syncwarp();
-      drain_wait(c, c.b(BDRAIN), 0);
+      drain_wait(c.abort, c.err, c.b(BDRAIN), 0);
     }
   } else {
     // ------------------------------------------- softmax + epilogue (2-5)
@@ -316,38 +328,34 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       for (int j = 0; j < kKvTile / 32; ++j) ptx::tmem_ld32(tS + s * kKvTile + j * 32, r + j * 32);
       ptx::tmem_wait_ld();
       const int key0 = kv0 + t * kKvTile;
-      float mx = neg_inf();
+      float mx = neg_inf();  // max of the raw scores (sm_scale > 0 keeps the order)
       if (key0 + kKvTile - 1 <= jmax) {  // every key of the tile is visible to this row
 #pragma unroll
-        for (int i = 0; i < kKvTile; ++i) {
-          const float x = __uint_as_float(r[i]) * sl2;
-          r[i] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
+        for (int i = 0; i < kKvTile; ++i) mx = fmaxf(mx, __uint_as_float(r[i]));
       } else {  // diagonal / last tile: mask keys past this row's last visible key
 #pragma unroll
         for (int i = 0; i < kKvTile; ++i) {
-          const float x = (key0 + i <= jmax) ? __uint_as_float(r[i]) * sl2 : neg_inf();
+          const float x = (key0 + i <= jmax) ? __uint_as_float(r[i]) : neg_inf();
           r[i] = __float_as_uint(x);
           mx = fmaxf(mx, x);
         }
       }
-      const float m_new = fmaxf(m_ref, mx);
+      const float m_new = fmaxf(m_ref, mx * sl2);
       const bool rescale = m_new > m_ref + kRescaleThreshold;
       float alpha = 1.f;
       if (rescale) {
         alpha = ptx::ex2(m_ref - m_new);
         m_ref = m_new;
       }
-      const float m_use = m_ref == neg_inf() ? 0.f : m_ref;
+      const float neg_m = m_ref == neg_inf() ? 0.f : -m_ref;
       float sum = 0.f;
-      uint32_t pk[kKvTile / 2];
+      // bf16 pairs of P overwrite the consumed scores in place: r[i/2] after r[i], r[i+1]
 #pragma unroll
       for (int i = 0; i < kKvTile; i += 2) {
-        const float p0 = ptx::ex2(__uint_as_float(r[i]) - m_use);
-        const float p1 = ptx::ex2(__uint_as_float(r[i + 1]) - m_use);
+        const float p0 = ptx::ex2(fmaf(__uint_as_float(r[i]), sl2, neg_m));
+        const float p1 = ptx::ex2(fmaf(__uint_as_float(r[i + 1]), sl2, neg_m));
         sum += p0 + p1;
-        pk[i / 2] = ptx::pack_bf16x2(p0, p1);
+        r[i / 2] = ptx::pack_bf16x2(p0, p1);
       }
       l = l * alpha + sum;
       if (t > 0) {
@@ -375,7 +383,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       for (int ch = 0; ch < kKvTile / 8; ++ch) {
         const int h = ch >> 3, cc = ch & 7;
         *reinterpret_cast<uint4*>(gP + h * C::kHalfBytes + row * 128 + ((cc ^ (row & 7)) << 4)) =
-            make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+            make_uint4(r[ch * 4], r[ch * 4 + 1], r[ch * 4 + 2], r[ch * 4 + 3]);
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
@@ -425,7 +433,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
 }
 
 // ------------------------------------------------------------------------
-// decode item: TMA page ring + mma.sync
+// decode item: whole-page TMA ring + mma.sync, one warp per kv head
 // ------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t keep_pair(uint32_t v, int k, int nvalid) {
   const uint32_t lo = k < nvalid ? 0x0000FFFFu : 0u;
@@ -436,13 +444,17 @@ __device__ __forceinline__ uint32_t keep_pair(uint32_t v, int k, int nvalid) {
 template <int D>
 __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, const Seg& sg,
                                             const KParams& p, uint32_t base, uint8_t* gb,
-                                            const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                            const CUtensorMap* tm_kd, const CUtensorMap* tm_vd,
                                             int warp, int lane) {
   using C = Cfg<D>;
   const int G = p.G;
+  const int HG = it.num_heads;                 // kv heads of the group (1, 2, 4 or 8)
   const int kv0 = it.kv_begin, kv1 = it.kv_end;
   const int npg = (kv1 - kv0 + kPageSize - 1) / kPageSize;
-  const uint32_t ring = base + C::kOffRing;
+  const int NS = p.dec_stages;
+  const int block = HG * C::kHeadBlock;        // K (or V) bytes of one page for the group
+  const int stage_bytes = 2 * block;
+  const uint32_t ring = base;
 
   if (warp == 0) {
     const uint64_t pol = ptx::policy_evict_first();  // each page is read once
@@ -453,212 +465,264 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
       const int pg = lane < n ? page_of(p, it.seg, kv0 / kPageSize + b0 + lane) : p.num_pages;
       for (int i = 0; i < n; ++i) {
         const int pi = b0 + i;
-        const int s = pi % kDecStages;
-        if (pi >= kDecStages && !(ok = wait_on(c, c.b(BEMPTY0 + s), ((pi / kDecStages) + 1) & 1)))
-          break;
+        const int s = pi % NS;
+        if (pi >= NS && !(ok = wait_on(c, c.b(BEMPTY0 + s), ((pi / NS) + 1) & 1))) break;
         const int pgi = __shfl_sync(0xffffffffu, pg, i);
         if (lane == 0) {
-          const uint32_t dst = ring + s * C::kStageBytes;
-          ptx::mbar_arrive_expect_tx(c.b(BFULL0 + s), C::kStageBytes);
-#pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
-            ptx::tma_load_5d(dst + h * kPageSize * 128, tm_k, c.b(BFULL0 + s), 0, h, it.kv_head, 0,
-                             pgi, pol);
-#pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
-            ptx::tma_load_5d(dst + C::kPageBytes + h * kPageSize * 128, tm_v, c.b(BFULL0 + s), 0,
-                             h, it.kv_head, 0, pgi, pol);
+          const uint32_t dst = ring + s * stage_bytes;
+          ptx::mbar_arrive_expect_tx(c.b(BFULL0 + s), stage_bytes);
+          ptx::tma_load_5d(dst, tm_kd, c.b(BFULL0 + s), 0, 0, 0, it.kv_head, pgi, pol);
+          ptx::tma_load_5d(dst + block, tm_vd, c.b(BFULL0 + s), 0, 0, 0, it.kv_head, pgi, pol);
         }
         __syncwarp();
         issued = pi + 1;
       }
     }
-    for (int s = 0; s < kDecStages && s < issued; ++s) {
-      const int last = s + ((issued - 1 - s) / kDecStages) * kDecStages;
-      drain_wait(c, c.b(BFULL0 + s), (last / kDecStages) & 1);
+    for (int s = 0; s < NS && s < issued; ++s) {
+      const int last = s + ((issued - 1 - s) / NS) * NS;
+      drain_wait(c.abort, c.err, c.b(BFULL0 + s), (last / NS) & 1);
     }
-  } else if (warp >= 2) {
-    const int cw = warp - 2;
-    const int gid = lane >> 2, tig = lane & 3;
-    const int R = it.q_count * G;
-    const int last_tok = it.q_count - 1;
-    const int tl = gid / G < last_tok ? gid / G : last_tok;
-    const int th = (gid + 8) / G < last_tok ? (gid + 8) / G : last_tok;
-    const int jlo = min(sg.hist + it.q_begin + tl, kv1 - 1);
-    const int jhi = min(sg.hist + it.q_begin + th, kv1 - 1);
-    const bool vlo = gid < R, vhi = gid + 8 < R;
-    const float sl2 = p.scale_log2;
+    return;
+  }
+  if (warp < 2) return;
 
-    // Q rows (row r = token r / G, head r % G of this kv head) as m16n8k16 A fragments
-    uint32_t qa[D / 16][4];
-    {
-      const uint32_t* qlo = reinterpret_cast<const uint32_t*>(
-          p.q + (static_cast<size_t>(sg.q_start + it.q_begin + gid / G) * p.hq + it.kv_head * G +
-                 gid % G) * D);
-      const uint32_t* qhi = reinterpret_cast<const uint32_t*>(
-          p.q + (static_cast<size_t>(sg.q_start + it.q_begin + (gid + 8) / G) * p.hq +
-                 it.kv_head * G + (gid + 8) % G) * D);
+  // ---------------------------------------------------- consumers (2-9)
+  const int cw = warp - 2;
+  const int hw = cw % HG;        // kv head (within the group) of this warp
+  const int ps = 8 / HG;         // warps sharing that head
+  const int po = cw / HG;        // this warp takes pages po, po + ps, ...
+  const int head = it.kv_head + hw;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int R = it.q_count * G;
+  const int last_tok = it.q_count - 1;
+  const int tl = gid / G < last_tok ? gid / G : last_tok;
+  const int th = (gid + 8) / G < last_tok ? (gid + 8) / G : last_tok;
+  const int jlo = min(sg.hist + it.q_begin + tl, kv1 - 1);
+  const int jhi = min(sg.hist + it.q_begin + th, kv1 - 1);
+  const bool vlo = gid < R, vhi = gid + 8 < R;
+  const float sl2 = p.scale_log2;
+
+  // Q rows (row r = token r / G, head r % G of this kv head) as m16n8k16 A fragments
+  uint32_t qa[D / 16][4];
+  {
+    const uint32_t* qlo = reinterpret_cast<const uint32_t*>(
+        p.q + (static_cast<size_t>(sg.q_start + it.q_begin + gid / G) * p.hq + head * G + gid % G) * D);
+    const uint32_t* qhi = reinterpret_cast<const uint32_t*>(
+        p.q + (static_cast<size_t>(sg.q_start + it.q_begin + (gid + 8) / G) * p.hq + head * G +
+               (gid + 8) % G) * D);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        qa[kk][0] = vlo ? qlo[kk * 8 + tig] : 0u;
-        qa[kk][1] = vhi ? qhi[kk * 8 + tig] : 0u;
-        qa[kk][2] = vlo ? qlo[kk * 8 + 4 + tig] : 0u;
-        qa[kk][3] = vhi ? qhi[kk * 8 + 4 + tig] : 0u;
-      }
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qa[kk][0] = vlo ? qlo[kk * 8 + tig] : 0u;
+      qa[kk][1] = vhi ? qhi[kk * 8 + tig] : 0u;
+      qa[kk][2] = vlo ? qlo[kk * 8 + 4 + tig] : 0u;
+      qa[kk][3] = vhi ? qhi[kk * 8 + 4 + tig] : 0u;
     }
-    float o[D / 8][4];
+  }
+  float o[D / 8][4];
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float mlo = neg_inf(), mhi = neg_inf(), llo = 0.f, lhi = 0.f;
-    bool ok = true;
-    const int mi = lane >> 3, rr = lane & 7;
-    for (int pi = cw; pi < npg; pi += 4) {
-      const int s = pi % kDecStages;
-      if (!(ok = wait_on(c, c.b(BFULL0 + s), (pi / kDecStages) & 1))) break;
-      const uint32_t kb = ring + s * C::kStageBytes;
-      const uint32_t vb = kb + C::kPageBytes;
-      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mlo = neg_inf(), mhi = neg_inf(), llo = 0.f, lhi = 0.f;
+  bool ok = true;
+  const int mi = lane >> 3, rr = lane & 7;
+  const uint32_t head_off = static_cast<uint32_t>(hw * C::kHeadBlock);
+  for (int pi = po; pi < npg; pi += ps) {
+    const int s = pi % NS;
+    if (!(ok = wait_on(c, c.b(BFULL0 + s), (pi / NS) & 1))) break;
+    const uint32_t kb = ring + s * stage_bytes + head_off;
+    const uint32_t vb = kb + block;
+    // two independent accumulator chains (even / odd k-steps) halve the MMA latency chain
+    float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float sb[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int h = kk >> 2, c0 = (kk & 3) * 2;
-        const int tk = (mi >> 1) * 8 + rr;  // matrices: (tok 0-7, c0) (0-7, c0+1) (8-15, c0) (8-15, c0+1)
-        const int ch = c0 + (mi & 1);
-        uint32_t b0, b1, b2, b3;
-        ptx::ldsm_x4(kb + h * kPageSize * 128 + tk * 128 + ((ch ^ (tk & 7)) << 4), b0, b1, b2, b3);
-        ptx::mma16816(sacc[0], qa[kk], b0, b1);
-        ptx::mma16816(sacc[1], qa[kk], b2, b3);
-      }
-      const int key0 = kv0 + pi * kPageSize;
-      float x[2][4];
-      float xlo = neg_inf(), xhi = neg_inf();
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int key = key0 + nt * 8 + tig * 2 + e;
-          x[nt][e] = key <= jlo ? sacc[nt][e] * sl2 : neg_inf();
-          x[nt][2 + e] = key <= jhi ? sacc[nt][2 + e] * sl2 : neg_inf();
-          xlo = fmaxf(xlo, x[nt][e]);
-          xhi = fmaxf(xhi, x[nt][2 + e]);
-        }
-      xlo = fmaxf(xlo, __shfl_xor_sync(0xffffffffu, xlo, 1));
-      xlo = fmaxf(xlo, __shfl_xor_sync(0xffffffffu, xlo, 2));
-      xhi = fmaxf(xhi, __shfl_xor_sync(0xffffffffu, xhi, 1));
-      xhi = fmaxf(xhi, __shfl_xor_sync(0xffffffffu, xhi, 2));
-      const float nlo = fmaxf(mlo, xlo), nhi = fmaxf(mhi, xhi);
-      if (nlo > mlo + kRescaleThreshold) {
-        const float a = ptx::ex2(mlo - nlo);
-        mlo = nlo;
-        llo *= a;
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) { o[i][0] *= a; o[i][1] *= a; }
-      }
-      if (nhi > mhi + kRescaleThreshold) {
-        const float a = ptx::ex2(mhi - nhi);
-        mhi = nhi;
-        lhi *= a;
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) { o[i][2] *= a; o[i][3] *= a; }
-      }
-      const float ulo = mlo == neg_inf() ? 0.f : mlo;
-      const float uhi = mhi == neg_inf() ? 0.f : mhi;
-      float pv[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        pv[nt][0] = ptx::ex2(x[nt][0] - ulo);
-        pv[nt][1] = ptx::ex2(x[nt][1] - ulo);
-        pv[nt][2] = ptx::ex2(x[nt][2] - uhi);
-        pv[nt][3] = ptx::ex2(x[nt][3] - uhi);
-        llo += pv[nt][0] + pv[nt][1];
-        lhi += pv[nt][2] + pv[nt][3];
-      }
-      uint32_t pa[4] = {ptx::pack_bf16x2(pv[0][0], pv[0][1]), ptx::pack_bf16x2(pv[0][2], pv[0][3]),
-                        ptx::pack_bf16x2(pv[1][0], pv[1][1]), ptx::pack_bf16x2(pv[1][2], pv[1][3])};
-      const int nvalid = kv1 - key0;
-#pragma unroll
-      for (int dd = 0; dd < D / 16; ++dd) {
-        const int h = dd >> 2, c0 = (dd & 3) * 2;
-        const int tk = (mi & 1) * 8 + rr;  // matrices: (tok 0-7, c0) (8-15, c0) (0-7, c0+1) (8-15, c0+1)
-        const int ch = c0 + (mi >> 1);
-        uint32_t v0, v1, v2, v3;
-        ptx::ldsm_x4_t(vb + h * kPageSize * 128 + tk * 128 + ((ch ^ (tk & 7)) << 4), v0, v1, v2, v3);
-        if (nvalid < kPageSize) {
-          // keys past the item's end: unused slots may hold NaN; P is 0 there
-          v0 = keep_pair(v0, tig * 2, nvalid);
-          v1 = keep_pair(v1, 8 + tig * 2, nvalid);
-          v2 = keep_pair(v2, tig * 2, nvalid);
-          v3 = keep_pair(v3, 8 + tig * 2, nvalid);
-        }
-        ptx::mma16816(o[2 * dd], pa, v0, v1);
-        ptx::mma16816(o[2 * dd + 1], pa, v2, v3);
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(c.b(BEMPTY0 + s));
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int h = kk >> 2, c0 = (kk & 3) * 2;
+      const int tk = (mi >> 1) * 8 + rr;  // matrices: (tok 0-7, c0) (0-7, c0+1) (8-15, c0) (8-15, c0+1)
+      const int ch = c0 + (mi & 1);
+      uint32_t b0, b1, b2, b3;
+      ptx::ldsm_x4(kb + h * kPageSize * 128 + tk * 128 + ((ch ^ (tk & 7)) << 4), b0, b1, b2, b3);
+      float(*acc)[4] = (kk & 1) ? sb : sa;
+      ptx::mma16816(acc[0], qa[kk], b0, b1);
+      ptx::mma16816(acc[1], qa[kk], b2, b3);
     }
-    // full row sums inside each quad
-    llo += __shfl_xor_sync(0xffffffffu, llo, 1);
-    llo += __shfl_xor_sync(0xffffffffu, llo, 2);
-    lhi += __shfl_xor_sync(0xffffffffu, lhi, 1);
-    lhi += __shfl_xor_sync(0xffffffffu, lhi, 2);
-    // merge the four warps' (m, l, O) through shared memory
-    float* mo = reinterpret_cast<float*>(gb + C::kOffMerge);
-    float* mm = mo + 4 * 16 * D;
-    float* ml = mm + 64;
-    float* mine = mo + cw * 16 * D;
+    const int key0 = kv0 + pi * kPageSize;
+    float x[2][4];
+    float xlo = neg_inf(), xhi = neg_inf();
 #pragma unroll
-    for (int nb = 0; nb < D / 8; ++nb) {
-      *reinterpret_cast<float2*>(mine + gid * D + nb * 8 + tig * 2) = make_float2(o[nb][0], o[nb][1]);
-      *reinterpret_cast<float2*>(mine + (gid + 8) * D + nb * 8 + tig * 2) = make_float2(o[nb][2], o[nb][3]);
-    }
-    if (tig == 0) {
-      mm[cw * 16 + gid] = mlo;
-      mm[cw * 16 + gid + 8] = mhi;
-      ml[cw * 16 + gid] = llo;
-      ml[cw * 16 + gid + 8] = lhi;
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    const int t = threadIdx.x - 64;
-    const int row = t >> 3;
-    const int d0 = (t & 7) * (D / 8);
-    float M = neg_inf();
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, mm[w * 16 + row]);
-    float wt[4], L = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float mw = mm[w * 16 + row];
-      wt[w] = mw == neg_inf() ? 0.f : ptx::ex2(mw - M);
-      L += wt[w] * ml[w * 16 + row];
-    }
-    if (row < R && ok && !*c.abort) {
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      float acc[D / 8];
-#pragma unroll
-      for (int d = 0; d < D / 8; ++d) {
-        float a = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) a += wt[w] * mo[w * 16 * D + row * D + d0 + d];
-        acc[d] = a * inv;
+      for (int e = 0; e < 2; ++e) {
+        const int key = key0 + nt * 8 + tig * 2 + e;
+        x[nt][e] = key <= jlo ? (sa[nt][e] + sb[nt][e]) * sl2 : neg_inf();
+        x[nt][2 + e] = key <= jhi ? (sa[nt][2 + e] + sb[nt][2 + e]) * sl2 : neg_inf();
+        xlo = fmaxf(xlo, x[nt][e]);
+        xhi = fmaxf(xhi, x[nt][2 + e]);
       }
-      const int tok = it.q_begin + row / G;
-      const int g = row - (row / G) * G;
-      const size_t orow = static_cast<size_t>(sg.q_start + tok) * p.hq + it.kv_head * G + g;
-      const float lse = L > 0.f ? (M + log2f(L)) * kLn2 : neg_inf();
-      if (it.part_row < 0) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + orow * D + d0);
+    xlo = fmaxf(xlo, __shfl_xor_sync(0xffffffffu, xlo, 1));
+    xlo = fmaxf(xlo, __shfl_xor_sync(0xffffffffu, xlo, 2));
+    xhi = fmaxf(xhi, __shfl_xor_sync(0xffffffffu, xhi, 1));
+    xhi = fmaxf(xhi, __shfl_xor_sync(0xffffffffu, xhi, 2));
+    const float nlo = fmaxf(mlo, xlo), nhi = fmaxf(mhi, xhi);
+    if (nlo > mlo + kRescaleThreshold) {
+      const float a = ptx::ex2(mlo - nlo);
+      mlo = nlo;
+      llo *= a;
 #pragma unroll
-        for (int d = 0; d < D / 8; d += 8)
-          *reinterpret_cast<uint4*>(dst + d / 2) =
-              make_uint4(ptx::pack_bf16x2(acc[d], acc[d + 1]), ptx::pack_bf16x2(acc[d + 2], acc[d + 3]),
-                         ptx::pack_bf16x2(acc[d + 4], acc[d + 5]), ptx::pack_bf16x2(acc[d + 6], acc[d + 7]));
-        if (p.lse && (t & 7) == 0) p.lse[orow] = lse;
+      for (int i = 0; i < D / 8; ++i) { o[i][0] *= a; o[i][1] *= a; }
+    }
+    if (nhi > mhi + kRescaleThreshold) {
+      const float a = ptx::ex2(mhi - nhi);
+      mhi = nhi;
+      lhi *= a;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) { o[i][2] *= a; o[i][3] *= a; }
+    }
+    const float ulo = mlo == neg_inf() ? 0.f : mlo;
+    const float uhi = mhi == neg_inf() ? 0.f : mhi;
+    float pv[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      pv[nt][0] = ptx::ex2(x[nt][0] - ulo);
+      pv[nt][1] = ptx::ex2(x[nt][1] - ulo);
+      pv[nt][2] = ptx::ex2(x[nt][2] - uhi);
+      pv[nt][3] = ptx::ex2(x[nt][3] - uhi);
+      llo += pv[nt][0] + pv[nt][1];
+      lhi += pv[nt][2] + pv[nt][3];
+    }
+    uint32_t pa[4] = {ptx::pack_bf16x2(pv[0][0], pv[0][1]), ptx::pack_bf16x2(pv[0][2], pv[0][3]),
+                      ptx::pack_bf16x2(pv[1][0], pv[1][1]), ptx::pack_bf16x2(pv[1][2], pv[1][3])};
+    const int nvalid = kv1 - key0;
+#pragma unroll
+    for (int dd = 0; dd < D / 16; ++dd) {
+      const int h = dd >> 2, c0 = (dd & 3) * 2;
+      const int tk = (mi & 1) * 8 + rr;  // matrices: (tok 0-7, c0) (8-15, c0) (0-7, c0+1) (8-15, c0+1)
+      const int ch = c0 + (mi >> 1);
+      uint32_t v0, v1, v2, v3;
+      ptx::ldsm_x4_t(vb + h * kPageSize * 128 + tk * 128 + ((ch ^ (tk & 7)) << 4), v0, v1, v2, v3);
+      if (nvalid < kPageSize) {
+        // keys past the item's end: unused slots may hold NaN; P is 0 there
+        v0 = keep_pair(v0, tig * 2, nvalid);
+        v1 = keep_pair(v1, 8 + tig * 2, nvalid);
+        v2 = keep_pair(v2, tig * 2, nvalid);
+        v3 = keep_pair(v3, 8 + tig * 2, nvalid);
+      }
+      ptx::mma16816(o[2 * dd], pa, v0, v1);
+      ptx::mma16816(o[2 * dd + 1], pa, v2, v3);
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(c.b(BEMPTY0 + s));
+  }
+  // full row sums inside each quad
+  llo += __shfl_xor_sync(0xffffffffu, llo, 1);
+  llo += __shfl_xor_sync(0xffffffffu, llo, 2);
+  lhi += __shfl_xor_sync(0xffffffffu, lhi, 1);
+  lhi += __shfl_xor_sync(0xffffffffu, lhi, 2);
+
+  const bool direct = it.part_row < 0;
+  if (ps == 1) {
+    // this warp alone saw its head's whole KV range: write from the fragments
+    if (!ok || *c.abort) return;
+    const float ilo = llo > 0.f ? 1.f / llo : 0.f;
+    const float ihi = lhi > 0.f ? 1.f / lhi : 0.f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int r = gid + 8 * half;
+      if (r >= R) continue;
+      const int tok = it.q_begin + r / G;
+      const int g = r - (r / G) * G;
+      const float inv = half ? ihi : ilo;
+      const size_t orow = static_cast<size_t>(sg.q_start + tok) * p.hq + head * G + g;
+      if (direct) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + orow * D);
+#pragma unroll
+        for (int nb = 0; nb < D / 8; ++nb)
+          dst[(nb * 8 + tig * 2) / 2] = ptx::pack_bf16x2(o[nb][2 * half] * inv, o[nb][2 * half + 1] * inv);
       } else {
-        float* dst = p.part_o + static_cast<size_t>(it.part_row + row) * D + d0;
+        float* dst = p.part_o + static_cast<size_t>(it.part_row + hw * it.part_head_stride + r) * D;
 #pragma unroll
-        for (int d = 0; d < D / 8; d += 4)
-          *reinterpret_cast<float4*>(dst + d) = make_float4(acc[d], acc[d + 1], acc[d + 2], acc[d + 3]);
-        if ((t & 7) == 0) p.part_lse[it.part_row + row] = lse;
+        for (int nb = 0; nb < D / 8; ++nb)
+          *reinterpret_cast<float2*>(dst + nb * 8 + tig * 2) =
+              make_float2(o[nb][2 * half] * inv, o[nb][2 * half + 1] * inv);
       }
+      if (tig == 0) {
+        const float m = half ? mhi : mlo;
+        const float L = half ? lhi : llo;
+        const float lse = L > 0.f ? (m + log2f(L)) * kLn2 : neg_inf();
+        if (direct) {
+          if (p.lse) p.lse[orow] = lse;
+        } else {
+          p.part_lse[it.part_row + hw * it.part_head_stride + r] = lse;
+        }
+      }
+    }
+    return;
+  }
+  // several warps per head: merge their (m, l, O) through shared memory.  The
+  // ring is idle once every consumer warp has passed the first barrier.
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  float* mo = reinterpret_cast<float*>(gb);           // [8 warps][16 rows][D]
+  float* mm = mo + 8 * 16 * D;                         // [8 warps][16 rows]
+  float* ml = mm + 8 * 16;
+  float* mine = mo + cw * 16 * D;
+#pragma unroll
+  for (int nb = 0; nb < D / 8; ++nb) {
+    *reinterpret_cast<float2*>(mine + gid * D + nb * 8 + tig * 2) = make_float2(o[nb][0], o[nb][1]);
+    *reinterpret_cast<float2*>(mine + (gid + 8) * D + nb * 8 + tig * 2) = make_float2(o[nb][2], o[nb][3]);
+  }
+  if (tig == 0) {
+    mm[cw * 16 + gid] = mlo;
+    mm[cw * 16 + gid + 8] = mhi;
+    ml[cw * 16 + gid] = llo;
+    ml[cw * 16 + gid + 8] = lhi;
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  if (po != 0 || !ok || *c.abort) return;
+  // warp (hw, po = 0) finishes head hw: lane -> row lane % 16, columns half (lane / 16)
+  const int r = lane & 15;
+  if (r >= R) return;
+  const int d0 = (lane >> 4) * (D / 2);
+  float M = neg_inf();
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (k < ps) M = fmaxf(M, mm[(hw + k * HG) * 16 + r]);
+  float wt[8], L = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    wt[k] = 0.f;
+    if (k < ps) {
+      const float mk = mm[(hw + k * HG) * 16 + r];
+      wt[k] = mk == neg_inf() ? 0.f : ptx::ex2(mk - M);
+      L += wt[k] * ml[(hw + k * HG) * 16 + r];
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int tok = it.q_begin + r / G;
+  const int g = r - (r / G) * G;
+  const size_t orow = static_cast<size_t>(sg.q_start + tok) * p.hq + head * G + g;
+  for (int d = 0; d < D / 2; d += 4) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k >= ps) break;
+      const float4 v = *reinterpret_cast<const float4*>(mo + ((hw + k * HG) * 16 + r) * D + d0 + d);
+      a[0] += wt[k] * v.x;
+      a[1] += wt[k] * v.y;
+      a[2] += wt[k] * v.z;
+      a[3] += wt[k] * v.w;
+    }
+    if (direct) {
+      uint2 pk2 = make_uint2(ptx::pack_bf16x2(a[0] * inv, a[1] * inv), ptx::pack_bf16x2(a[2] * inv, a[3] * inv));
+      *reinterpret_cast<uint2*>(p.out + orow * D + d0 + d) = pk2;
+    } else {
+      *reinterpret_cast<float4*>(p.part_o + static_cast<size_t>(it.part_row + hw * it.part_head_stride + r) * D + d0 + d) =
+          make_float4(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv);
+    }
+  }
+  if (lane < 16) {
+    const float lse = L > 0.f ? (M + log2f(L)) * kLn2 : neg_inf();
+    if (direct) {
+      if (p.lse) p.lse[orow] = lse;
+    } else {
+      p.part_lse[it.part_row + hw * it.part_head_stride + r] = lse;
     }
   }
 }
@@ -667,7 +731,9 @@ template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     mixed_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, const KParams p) {
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_kd,
+                          const __grid_constant__ CUtensorMap tm_vd, const KParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -683,16 +749,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const bool prefill = it.kind == kPrefillItem;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(c.b(i), 1);
-    ptx::mbar_init(c.b(BP), 128);
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t count = 1;
+      if (i >= BK0 && i < BV0 + 2) count = 2;         // two producer warps per K / V tile
+      if (i == BP) count = 128;                        // every softmax thread
+      if (i >= BEMPTY0) count = prefill ? 1 : it.num_heads;  // one warp per head reads a stage
+      ptx::mbar_init(c.b(i), count);
+    }
     *c.abort = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    if (prefill) ptx::prefetch_tmap(&tm_q);
-    ptx::prefetch_tmap(&tm_k);
-    ptx::prefetch_tmap(&tm_v);
+    if (prefill) {
+      ptx::prefetch_tmap(&tm_q);
+    } else {
+      ptx::prefetch_tmap(&tm_kd);
+      ptx::prefetch_tmap(&tm_vd);
+    }
   }
+  if (prefill && warp >= 6 && lane == 0) ptx::prefetch_tmap(warp < 8 ? &tm_k : &tm_v);
   if (prefill && warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
     ptx::tmem_relinquish();
@@ -710,7 +785,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (prefill) {
     prefill_item<D>(c, it, sg, p, base, gb, *tmem_slot, &tm_q, &tm_k, &tm_v, warp, lane);
   } else {
-    decode_item<D>(c, it, sg, p, base, gb, &tm_k, &tm_v, warp, lane);
+    decode_item<D>(c, it, sg, p, base, gb, &tm_kd, &tm_vd, warp, lane);
   }
 
   ptx::tc_fence_before();
@@ -757,12 +832,26 @@ bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
   return true;
 }
 
+// Decode ring stages for head group HG: as many as fit, a multiple of the
+// warps that share one head (8 / HG) so each stage is always read by the same
+// warps (mbarrier parity waits must never run a phase ahead).
+template <int D>
+int decode_stages(int HG) {
+  const int stage = 2 * HG * Cfg<D>::kHeadBlock;
+  const int per_head = kDecodeMaxHeads / HG;
+  int ns = kDecRingBytes / stage;
+  if (ns > kMaxDecStages) ns = kMaxDecStages;
+  ns -= ns % per_head;
+  return ns;
+}
+
 template <int D>
 int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   using C = Cfg<D>;
   const int G = a.num_q_heads / a.num_kv_heads;
   const int TQ = kTileRows / G;
-  alignas(64) CUtensorMap tq, tk, tv;
+  const int HG = decode_head_group(a.num_kv_heads);
+  alignas(64) CUtensorMap tq, tk, tv, tkd, tvd;
   {
     cuuint64_t dims[4] = {64, (cuuint64_t)(D / 64), (cuuint64_t)a.num_q_heads,
                           (cuuint64_t)(a.total_q > 0 ? a.total_q : 1)};
@@ -771,6 +860,7 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
     if (!encode(&tq, a.q, 4, dims, strides, box, "q")) return -1;
   }
   {
+    // one 64-column panel of one kv head of one page: dims {d, panel, head, token, page}
     cuuint64_t dims[5] = {64, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads,
                           (cuuint64_t)a.page_size, (cuuint64_t)a.num_pages};
     cuuint64_t strides[4] = {128, (cuuint64_t)D * 2, (cuuint64_t)a.num_kv_heads * D * 2,
@@ -778,6 +868,17 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
     cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)a.page_size, 1};
     if (!encode(&tk, a.k_cache, 5, dims, strides, box, "k_cache")) return -1;
     if (!encode(&tv, a.v_cache, 5, dims, strides, box, "v_cache")) return -1;
+  }
+  {
+    // a whole page for HG kv heads, dims ordered {d, token, panel, head, page}
+    // so that shared memory receives [head][panel][token][64]
+    cuuint64_t dims[5] = {64, (cuuint64_t)a.page_size, (cuuint64_t)(D / 64),
+                          (cuuint64_t)a.num_kv_heads, (cuuint64_t)a.num_pages};
+    cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * D * 2, 128, (cuuint64_t)D * 2,
+                             (cuuint64_t)a.page_size * a.num_kv_heads * D * 2};
+    cuuint32_t box[5] = {64, (cuuint32_t)a.page_size, (cuuint32_t)(D / 64), (cuuint32_t)HG, 1};
+    if (!encode(&tkd, a.k_cache, 5, dims, strides, box, "k_cache pages")) return -1;
+    if (!encode(&tvd, a.v_cache, 5, dims, strides, box, "v_cache pages")) return -1;
   }
   KParams kp;
   kp.items = a.items;
@@ -794,11 +895,12 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   kp.num_pages = a.num_pages;
   kp.hq = a.num_q_heads;
   kp.G = G;
+  kp.dec_stages = decode_stages<D>(HG);
   kp.scale_log2 = a.sm_scale * kLog2e;
   cudaError_t e = cudaFuncSetAttribute(mixed_attn_fwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return static_cast<int>(e);
-  mixed_attn_fwd_kernel<D><<<a.num_items, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, kp);
+  mixed_attn_fwd_kernel<D><<<a.num_items, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, tkd, tvd, kp);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -70,10 +70,13 @@ mcp_status validate_desc(const mcp_attn_desc* d) {
     return fail(MCP_ERR_UNSUPPORTED, "page_size %d (built: 16)", d->page_size);
   if (d->num_q_heads / d->num_kv_heads > mcp::kTileRows)
     return fail(MCP_ERR_UNSUPPORTED, "group size %d > 128", d->num_q_heads / d->num_kv_heads);
+  if (d->num_kv_heads > 32767)
+    return fail(MCP_ERR_UNSUPPORTED, "num_kv_heads %d > 32767", d->num_kv_heads);
   if (d->num_pages <= 0) return fail(MCP_ERR_INVALID_ARG, "num_pages %d <= 0", d->num_pages);
   if (d->num_seqs > 0 && d->max_pages_per_seq <= 0)
     return fail(MCP_ERR_INVALID_ARG, "max_pages_per_seq %d <= 0", d->max_pages_per_seq);
-  if (!std::isfinite(d->sm_scale)) return fail(MCP_ERR_INVALID_ARG, "sm_scale is not finite");
+  if (!std::isfinite(d->sm_scale) || d->sm_scale <= 0.f)
+    return fail(MCP_ERR_INVALID_ARG, "sm_scale must be finite and > 0");
   return MCP_OK;
 }
 
@@ -123,6 +126,7 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
   const int G = d.num_q_heads / d.num_kv_heads;
   const int TQ = mcp::kTileRows / G;
   const int H = d.num_kv_heads;
+  const int HG = mcp::decode_head_group(H);
   const int dopt = o ? o->decode_split_tokens : 0;
   const int popt = o ? o->prefill_split_tokens : 0;
 
@@ -134,7 +138,7 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
       if (lq * G <= mcp::kDecodeMaxRows) {
         int64_t k, z;
         even_split(lk, ds, mcp::kPageSize, &k, &z);
-        n += k * H;
+        n += k * (H / HG);
       } else {
         for (int64_t qb = 0; qb < lq; qb += TQ) {
           const int64_t vis = lk - lq + std::min<int64_t>(lq, qb + TQ);
@@ -147,31 +151,38 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
     return n;
   };
 
-  int64_t ds = dopt > 0 ? round_up(dopt, mcp::kPageSize) : 8192;
+  // Decode splits: about eight decode items per SM (each item streams its KV
+  // range for a whole kv-head group), never below 1024 tokens.
+  int64_t ds;
+  if (dopt > 0) {
+    ds = round_up(dopt, mcp::kPageSize);
+  } else {
+    int64_t dec_tokens = 0;
+    for (int s = 0; s < d.num_seqs; ++s) {
+      const int64_t lq = cu[s + 1] - cu[s];
+      if (lq > 0 && lq * G <= mcp::kDecodeMaxRows) dec_tokens += sk[s] * (H / HG);
+    }
+    ds = std::max<int64_t>(1024, round_up(cdiv(dec_tokens, 8LL * num_sms), mcp::kPageSize));
+  }
   int64_t ps = popt > 0 ? round_up(popt, mcp::kKvTile) : 32768;
   while (count(ds, ps) < 2LL * num_sms) {
     bool changed = false;
-    if (dopt <= 0 && ds > 1024) { ds /= 2; changed = true; }
+    if (dopt <= 0 && ds > 1024) { ds = std::max<int64_t>(1024, ds / 2); changed = true; }
     if (popt <= 0 && ps > 2048) { ps /= 2; changed = true; }
     if (!changed) break;
   }
   b.dsplit = static_cast<int>(ds);
   b.psplit = static_cast<int>(ps);
 
-  // Rough per-SM cost model (ns) used only for ordering: a decode key-head
-  // streams 4*D bytes of K/V at ~45 GB/s per SM; a tensor-core key-tile does
-  // 4*128*D flops at ~6 TFLOP/s per SM.
+  // Rough per-SM cost model (ns) used only for ordering: a decode key streams
+  // 4*D bytes of K/V per kv head at ~45 GB/s per SM; a tensor-core key-tile
+  // does 4*128*D flops at ~6 TFLOP/s per SM.
   struct Entry {
     mcp::WorkItem it;
     double cost;
     int64_t group;
   };
   std::vector<Entry> dec, pre;
-  struct Group {
-    int64_t id;
-    double cost;
-  };
-  std::vector<Group> groups;
   for (int s = 0; s < d.num_seqs; ++s) {
     const int64_t lq = cu[s + 1] - cu[s], lk = sk[s], hist = lk - lq;
     if (lq == 0) continue;
@@ -179,20 +190,29 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
       int64_t n, sz;
       even_split(lk, ds, mcp::kPageSize, &n, &sz);
       const int rows = static_cast<int>(lq * G);
-      for (int h = 0; h < H; ++h) {
+      for (int h0 = 0; h0 < H; h0 += HG) {
         int64_t base = -1;
         if (n > 1) {
+          // head j of the group, split k: partial rows base + j*n*rows + k*rows
           base = b.part_rows;
-          b.part_rows += n * rows;
-          b.comb.push_back({s, h, 0, static_cast<int32_t>(lq), static_cast<int32_t>(n),
-                            static_cast<int32_t>(base), rows, 0});
+          b.part_rows += n * rows * HG;
+          for (int j = 0; j < HG; ++j)
+            b.comb.push_back({s, h0 + j, 0, static_cast<int32_t>(lq), static_cast<int32_t>(n),
+                              static_cast<int32_t>(base + j * n * rows), rows, 0});
         }
         for (int64_t k = 0; k < n; ++k) {
-          mcp::WorkItem it{s, h, mcp::kDecodeItem, 0, static_cast<int32_t>(lq),
-                           static_cast<int32_t>(k * sz),
-                           static_cast<int32_t>(std::min(lk, (k + 1) * sz)),
-                           static_cast<int32_t>(n > 1 ? base + k * rows : -1)};
-          dec.push_back({it, (it.kv_end - it.kv_begin) * 4.0 * d.head_dim / 45.0, 0});
+          mcp::WorkItem it;
+          it.seg = s;
+          it.kv_head = static_cast<int16_t>(h0);
+          it.kind = mcp::kDecodeItem;
+          it.num_heads = static_cast<int8_t>(HG);
+          it.q_begin = 0;
+          it.q_count = static_cast<int32_t>(lq);
+          it.kv_begin = static_cast<int32_t>(k * sz);
+          it.kv_end = static_cast<int32_t>(std::min(lk, (k + 1) * sz));
+          it.part_row = static_cast<int32_t>(n > 1 ? base + k * rows : -1);
+          it.part_head_stride = static_cast<int32_t>(n * rows);
+          dec.push_back({it, (it.kv_end - it.kv_begin) * 4.0 * d.head_dim * HG / 45.0, 0});
         }
       }
     } else {
@@ -211,10 +231,17 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
                               static_cast<int32_t>(n), static_cast<int32_t>(base), rows, 0});
           }
           for (int64_t k = 0; k < n; ++k) {
-            mcp::WorkItem it{s, h, mcp::kPrefillItem, static_cast<int32_t>(qb),
-                             static_cast<int32_t>(qc), static_cast<int32_t>(k * sz),
-                             static_cast<int32_t>(std::min(vis, (k + 1) * sz)),
-                             static_cast<int32_t>(n > 1 ? base + k * rows : -1)};
+            mcp::WorkItem it;
+            it.seg = s;
+            it.kv_head = static_cast<int16_t>(h);
+            it.kind = mcp::kPrefillItem;
+            it.num_heads = 1;
+            it.q_begin = static_cast<int32_t>(qb);
+            it.q_count = static_cast<int32_t>(qc);
+            it.kv_begin = static_cast<int32_t>(k * sz);
+            it.kv_end = static_cast<int32_t>(std::min(vis, (k + 1) * sz));
+            it.part_row = static_cast<int32_t>(n > 1 ? base + k * rows : -1);
+            it.part_head_stride = 0;
             const double tiles = static_cast<double>(cdiv(it.kv_end - it.kv_begin, mcp::kKvTile));
             // tiles reading the same K/V (same segment, kv head, split) share a group
             const int64_t gid = (static_cast<int64_t>(s) * H + h) * 4096 + k;

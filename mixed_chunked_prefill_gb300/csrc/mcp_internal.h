@@ -9,22 +9,32 @@ namespace mcp {
 
 enum ItemKind : int32_t { kDecodeItem = 0, kPrefillItem = 1 };
 
-constexpr int kDecodeMaxRows = 16;   // query rows of a decode item: one m16 MMA tile
+constexpr int kDecodeMaxRows = 16;   // query rows of one kv head on the decode path (m16 tile)
+constexpr int kDecodeMaxHeads = 8;   // kv heads one decode item covers (one consumer warp each)
 constexpr int kTileRows = 128;       // query rows of a tensor-core tile (TMEM lanes)
 constexpr int kKvTile = 128;         // keys per tensor-core KV tile
 constexpr int kPageSize = 16;        // tokens per KV page supported by the kernels
-constexpr int kFwdThreads = 192;     // 6 warps: TMA producer, MMA issuer, 4 compute
+constexpr int kFwdThreads = 320;     // 10 warps: TMA producer, MMA issuer, 8 compute / producer
+
+// kv heads covered by one decode item: the largest power of two <= 8 dividing H_kv
+inline int decode_head_group(int num_kv_heads) {
+  int g = 1;
+  while (g * 2 <= kDecodeMaxHeads && num_kv_heads % (g * 2) == 0) g *= 2;
+  return g;
+}
 
 // One unit of work of the fused kernel (one CTA).  32 bytes.
 struct WorkItem {
-  int32_t seg;       // segment index in the stream
-  int32_t kv_head;   // kv head; the item covers its G query heads
-  int32_t kind;      // ItemKind
-  int32_t q_begin;   // first query token of the item, counted inside the segment
-  int32_t q_count;   // query tokens covered
-  int32_t kv_begin;  // first key position (multiple of 16, or of 128 for prefill)
-  int32_t kv_end;    // one past the last key position the item reads
-  int32_t part_row;  // -1: write out/lse directly; else first row in the partial buffers
+  int32_t seg;         // segment index in the stream
+  int16_t kv_head;     // first kv head covered
+  int8_t kind;         // ItemKind
+  int8_t num_heads;    // kv heads covered (decode: the head group; tensor-core tile: 1)
+  int32_t q_begin;     // first query token of the item, counted inside the segment
+  int32_t q_count;     // query tokens covered
+  int32_t kv_begin;    // first key position (multiple of 16, or of 128 for tiles)
+  int32_t kv_end;      // one past the last key position the item reads
+  int32_t part_row;    // -1: write out/lse directly; else first partial row of the first head
+  int32_t part_head_stride;  // partial rows between consecutive kv heads of the item
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
 

@@ -9,9 +9,9 @@ import numpy as np
 import mixed_chunked_prefill_gb300 as mcp
 from mixed_chunked_prefill_gb300 import _capi
 
-ITEM = np.dtype([("seg", "<i4"), ("kv_head", "<i4"), ("kind", "<i4"), ("q_begin", "<i4"),
-                 ("q_count", "<i4"), ("kv_begin", "<i4"), ("kv_end", "<i4"),
-                 ("part_row", "<i4")])
+ITEM = np.dtype([("seg", "<i4"), ("kv_head", "<i2"), ("kind", "i1"), ("num_heads", "i1"),
+                 ("q_begin", "<i4"), ("q_count", "<i4"), ("kv_begin", "<i4"), ("kv_end", "<i4"),
+                 ("part_row", "<i4"), ("part_head_stride", "<i4")])
 COMB = np.dtype([("seg", "<i4"), ("kv_head", "<i4"), ("q_begin", "<i4"), ("q_count", "<i4"),
                  ("num_splits", "<i4"), ("part_row", "<i4"), ("rows", "<i4"), ("pad", "<i4")])
 

@@ -203,9 +203,13 @@ def check_plan_covers(w, items, comb, plan):
     cu, _, _, _ = oracle.segment_layout(w.q_lens, w.k_lens)
     assert plan.num_items == len(items)
     assert plan.num_decode_items + plan.num_prefill_items == len(items)
+    assert (items["kind"] == 0).sum() == plan.num_decode_items
     cover = {}
+    HG = 1
+    while HG * 2 <= 8 and w.num_kv_heads % (HG * 2) == 0:
+        HG *= 2
     for it in items:
-        s, h = int(it["seg"]), int(it["kv_head"])
+        s = int(it["seg"])
         lq, lk = w.q_lens[s], w.k_lens[s]
         assert 0 <= it["q_begin"] and it["q_begin"] + it["q_count"] <= lq and it["q_count"] > 0
         assert 0 <= it["kv_begin"] < it["kv_end"] <= lk
@@ -214,11 +218,16 @@ def check_plan_covers(w, items, comb, plan):
         if it["kind"] == 0:
             assert it["q_count"] * G <= 16 and it["kv_begin"] % 16 == 0
             assert it["q_begin"] == 0 and it["q_count"] == lq
+            assert it["num_heads"] == HG and it["kv_head"] % HG == 0
         else:
             assert it["q_count"] * G <= 128 and it["kv_begin"] % 128 == 0
             assert it["q_count"] * G > 16 or lq * G > 16
-        key = (s, h, int(it["q_begin"]), int(it["q_count"]))
-        cover.setdefault(key, []).append((int(it["kv_begin"]), int(it["kv_end"]), int(it["part_row"])))
+            assert it["num_heads"] == 1
+        for j in range(int(it["num_heads"])):
+            h = int(it["kv_head"]) + j
+            part = -1 if it["part_row"] < 0 else int(it["part_row"]) + j * int(it["part_head_stride"])
+            key = (s, h, int(it["q_begin"]), int(it["q_count"]))
+            cover.setdefault(key, []).append((int(it["kv_begin"]), int(it["kv_end"]), part))
     # each row group: KV ranges tile [0, vis_end)
     rows_seen = {}
     for (s, h, qb, qc), ranges in cover.items():
@@ -303,7 +312,8 @@ def test_planner_balance_bound_big_configs():
         cu, _, _, _ = oracle.segment_layout(w.q_lens, w.k_lens)
         st, plan, items, comb = plan_host(desc_for(w), cu, w.k_lens)
         D = w.head_dim
-        cost = np.where(items["kind"] == 0, (items["kv_end"] - items["kv_begin"]) * 4.0 * D / 45.0,
+        cost = np.where(items["kind"] == 0,
+                        (items["kv_end"] - items["kv_begin"]) * 4.0 * D * items["num_heads"] / 45.0,
                         300.0 + np.ceil((items["kv_end"] - items["kv_begin"]) / 128)
                         * 4.0 * 128 * 128 * D / 6000.0)
         import heapq
