@@ -59,9 +59,12 @@ struct Cfg {
   // tensor-core item
   static constexpr int kQBytes = kHalves * kHalfBytes;
   static constexpr int kKvBytes = kHalves * kHalfBytes;  // one K (or V) tile of 128 keys
+  static constexpr int kKStages = 3;  // K tile t is free once Q K^T(t) is done
+  static constexpr int kVStages = 2;  // V tile t is free once P V(t) is done
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kQBytes;  // stage s: K at kOffK + 2*s*kKvBytes, V after it
-  static constexpr int kOffP = kOffK + 4 * kKvBytes;
+  static constexpr int kOffK = kQBytes;                          // K stage s at kOffK + s*kKvBytes
+  static constexpr int kOffV = kOffK + kKStages * kKvBytes;      // V stage s at kOffV + s*kKvBytes
+  static constexpr int kOffP = kOffV + kVStages * kKvBytes;
   static constexpr int kPBytes = 2 * kHalfBytes;  // P: 128 rows x 128 keys bf16
   static constexpr int kPrefillBytes = kOffP + kPBytes;
   // decode item: ring of [K block | V block], block = [head][panel][16 tokens][128 B]
@@ -72,19 +75,21 @@ struct Cfg {
   static constexpr int kDataBytes = kPrefillBytes > kDecRingBytes ? kPrefillBytes : kDecRingBytes;
   static constexpr int kOffBar = (kDataBytes + 1023) & ~1023;
   static constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // barriers/flags + alignment slack
+  static_assert(kSmemBytes <= 232448, "227 KB dynamic shared memory limit");
 };
 
 // barrier slots
 enum : int {
   BQ = 0,        // Q tile landed
-  BK0 = 1,       // K tile of stage s landed (BK0 + s); two producer warps arrive
-  BV0 = 3,       // V tile of stage s landed; two producer warps arrive
-  BE0 = 5,       // stage s free again (MMA done with K and V)
-  BS0 = 7,       // S buffer s holds Q K^T of the current tile
-  BP = 9,        // P of the current tile written (128 softmax threads)
-  BPV = 10,      // P V of the current tile accumulated into O
-  BDRAIN = 11,   // all MMAs of the CTA finished
-  BFULL0 = 12,   // decode ring stage landed (12 .. 12+kMaxDecStages-1)
+  BK0 = 1,       // K stage s landed (BK0 + s, s < 3); two producer warps arrive
+  BKE0 = 4,      // K stage s free again (Q K^T done)
+  BV0 = 7,       // V stage s landed (s < 2); two producer warps arrive
+  BVE0 = 9,      // V stage s free again (P V done)
+  BS0 = 11,      // S buffer s holds Q K^T of the current tile
+  BP = 13,       // P of the current tile written (128 softmax threads)
+  BPV = 14,      // P V of the current tile accumulated into O
+  BDRAIN = 15,   // all MMAs of the CTA finished
+  BFULL0 = 16,   // decode ring stage landed (16 .. 16+kMaxDecStages-1)
   BEMPTY0 = BFULL0 + kMaxDecStages,  // decode ring stage free
   kNumBars = BEMPTY0 + kMaxDecStages
 };
@@ -183,8 +188,8 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
   const int ntiles = (kv1 - kv0 + kKvTile - 1) / kKvTile;
   const uint32_t sQ = base + C::kOffQ;
   const uint32_t sP = base + C::kOffP;
-  auto sK = [&](int s) { return base + C::kOffK + static_cast<uint32_t>(2 * s * C::kKvBytes); };
-  auto sV = [&](int s) { return sK(s) + C::kKvBytes; };
+  auto sK = [&](int s) { return base + C::kOffK + static_cast<uint32_t>(s * C::kKvBytes); };
+  auto sV = [&](int s) { return base + C::kOffV + static_cast<uint32_t>(s * C::kKvBytes); };
   constexpr int kPages = kKvTile / kPageSize;  // 8 pages per tile
 
   if (warp == 0) {
@@ -205,10 +210,12 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     const int pg0 = (pr & 1) * (kPages / 2);
     const CUtensorMap* tm = isK ? tm_k : tm_v;
     const uint64_t pol = ptx::policy_evict_last();  // other q tiles re-read these K/V
+    const int NS = isK ? C::kKStages : C::kVStages;
+    const int full0 = isK ? BK0 : BV0, empty0 = isK ? BKE0 : BVE0;
     int t = 0;
     for (; t < ntiles; ++t) {
-      const int s = t & 1;
-      if (t >= 2 && !wait_on(c, c.b(BE0 + s), ((t >> 1) + 1) & 1)) break;
+      const int s = t % NS;
+      if (t >= NS && !wait_on(c, c.b(empty0 + s), ((t / NS) + 1) & 1)) break;
       const int key0 = kv0 + t * kKvTile;
       int npg = (kv1 - key0 + kPageSize - 1) / kPageSize;  // pages of the tile inside the item
       const int mine = lane < kPages / 2 && pg0 + lane < npg;
@@ -217,7 +224,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
 #pragma unroll
       for (int i = 0; i < kPages / 2; ++i) pgs[i] = __shfl_sync(0xffffffffu, pg, i);
       if (lane == 0) {
-        const uint32_t bar = c.b((isK ? BK0 : BV0) + s);
+        const uint32_t bar = c.b(full0 + s);
         const uint32_t dst = isK ? sK(s) : sV(s);
         ptx::mbar_arrive_expect_tx(bar, C::kKvBytes / 2);
 #pragma unroll
@@ -230,9 +237,9 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       __syncwarp();
     }
     // drain: the last tile this warp issued into each stage
-    for (int s = 0; s < 2; ++s) {
-      const int last = (t - 1 - s) >= 0 ? (t - 1 - ((t - 1 - s) & 1)) : -1;
-      if (last >= 0) drain_wait(c.abort, c.err, c.b((isK ? BK0 : BV0) + s), (last >> 1) & 1);
+    for (int s = 0; s < NS && s < t; ++s) {
+      const int last = s + ((t - 1 - s) / NS) * NS;
+      drain_wait(c.abort, c.err, c.b(full0 + s), (last / NS) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
@@ -242,17 +249,18 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     const uint32_t tO = tmem + 256;  // O: columns [256, 256 + D)
     bool issued = false;
     auto qk = [&](int t) -> bool {
-      const int s = t & 1;
-      if (!wait_on(c, c.b(BK0 + s), (t >> 1) & 1)) return false;
+      const int s = t % C::kKStages;
+      if (!wait_on(c, c.b(BK0 + s), (t / C::kKStages) & 1)) return false;
       ptx::tc_fence_after();
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-          ptx::mma_ss(tS + s * kKvTile, ptx::sdesc_sw128(sQ + off, 16, 1024),
+          ptx::mma_ss(tS + (t & 1) * kKvTile, ptx::sdesc_sw128(sQ + off, 16, 1024),
                       ptx::sdesc_sw128(sK(s) + off, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(c.b(BS0 + s));
+        ptx::mma_commit(c.b(BS0 + (t & 1)));
+        ptx::mma_commit(c.b(BKE0 + s));
       }
       __syncwarp();
       issued = true;
@@ -263,8 +271,8 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     for (int t = 0; ok && t < ntiles; ++t) {
       if (t + 1 < ntiles && !(ok = qk(t + 1))) break;
       if (!(ok = wait_on(c, c.b(BP), t & 1))) break;
-      const int s = t & 1;
-      if (!(ok = wait_on(c, c.b(BV0 + s), (t >> 1) & 1))) break;
+      const int s = t % C::kVStages;
+      if (!(ok = wait_on(c, c.b(BV0 + s), (t / C::kVStages) & 1))) break;
       const int nval = kv1 - (kv0 + t * kKvTile);
       if (nval < kKvTile && (nval & (kPageSize - 1))) {
         // Rows past the item's last key inside its last page may be unused
@@ -292,7 +300,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
                       (t > 0 || kk > 0) ? 1u : 0u);
         }
         ptx::mma_commit(c.b(BPV));
-        ptx::mma_commit(c.b(BE0 + s));
+        ptx::mma_commit(c.b(BVE0 + s));
       }
       __syncwarp();
     }
@@ -751,7 +759,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;
-      if (i >= BK0 && i < BV0 + 2) count = 2;         // two producer warps per K / V tile
+      if ((i >= BK0 && i < BK0 + 3) || (i >= BV0 && i < BV0 + 2)) count = 2;  // two producer warps
       if (i == BP) count = 128;                        // every softmax thread
       if (i >= BEMPTY0) count = prefill ? 1 : it.num_heads;  // one warp per head reads a stage
       ptx::mbar_init(c.b(i), count);

@@ -26,6 +26,8 @@ SEED_BASE = 20261202
 
 # name -> (index, description).  The index offsets the seed.
 CONFIG_NAMES = ["tiny", "worked", "balanced", "decode-heavy", "long-context"]
+# small single-kind workloads for kernel profiles (larger than L2, a few GB at most)
+PROFILE_NAMES = ["decode-32x16k", "chunk-512x16k"]
 
 DESCRIPTIONS = {
     "tiny": "tiny mixed step: 4 q / 4 kv heads, head_dim 64, page 16; decodes ctx 121 and 46, "
@@ -38,6 +40,9 @@ DESCRIPTIONS = {
                     "32768 history; 64 q / 8 kv heads, head_dim 128, page 16",
     "long-context": "long-context: 64 decodes ctx U[65536,131072] + one 2048-token chunk after "
                     "126976 history; 32 q / 8 kv heads, head_dim 128, page 16",
+    "decode-32x16k": "decode only: 32 decodes ctx 16384; 64 q / 8 kv heads, head_dim 128, page 16",
+    "chunk-512x16k": "chunk only: one 512-token chunk after 16384 history; 32 q / 8 kv heads, "
+                     "head_dim 128, page 16",
 }
 
 
@@ -165,7 +170,14 @@ def make_workload_from_lengths(name, num_q_heads, num_kv_heads, head_dim, page_s
 
 
 def make_workload(name: str, seed_offset: int = 0) -> Workload:
-    """One of the five named workloads, seeded with SEED_BASE + its index."""
+    """One of the named workloads, seeded with SEED_BASE + its index."""
+    if name in PROFILE_NAMES:
+        seed = SEED_BASE + 100 + PROFILE_NAMES.index(name) + seed_offset
+        if name == "decode-32x16k":
+            return make_workload_from_lengths(name, 64, 8, 128, 16, 1.0 / math.sqrt(128),
+                                              [1] * 32, [16384] * 32, seed)
+        return make_workload_from_lengths(name, 32, 8, 128, 16, 1.0 / math.sqrt(128),
+                                          [512], [16384 + 512], seed)
     idx = CONFIG_NAMES.index(name)
     seed = SEED_BASE + idx + seed_offset
     rng = np.random.Generator(np.random.PCG64(seed))
