@@ -59,14 +59,12 @@ struct Cfg {
   // tensor-core item
   static constexpr int kQBytes = kHalves * kHalfBytes;
   static constexpr int kKvBytes = kHalves * kHalfBytes;  // one K (or V) tile of 128 keys
-  static constexpr int kKStages = 3;  // K tile t is free once Q K^T(t) is done
-  static constexpr int kVStages = 2;  // V tile t is free once P V(t) is done
+  static constexpr int kKStages = 3;  // K and V tiles of tile t share stage t % 3,
+  static constexpr int kVStages = 3;  // released together once P V(t) is done
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kQBytes;                          // K stage s at kOffK + s*kKvBytes
   static constexpr int kOffV = kOffK + kKStages * kKvBytes;      // V stage s at kOffV + s*kKvBytes
-  static constexpr int kOffP = kOffV + kVStages * kKvBytes;
-  static constexpr int kPBytes = 2 * kHalfBytes;  // P: 128 rows x 128 keys bf16
-  static constexpr int kPrefillBytes = kOffP + kPBytes;
+  static constexpr int kPrefillBytes = kOffV + kVStages * kKvBytes;  // P lives in TMEM
   // decode item: ring of [K block | V block], block = [head][panel][16 tokens][128 B]
   static constexpr int kHeadBlock = kHalves * kPageSize * 128;
   static constexpr int kMergeBytes = 8 * 16 * D * 4 + 2 * 8 * 16 * 4;  // reuses the ring
@@ -81,14 +79,13 @@ struct Cfg {
 // barrier slots
 enum : int {
   BQ = 0,        // Q tile landed
-  BK0 = 1,       // K stage s landed (BK0 + s, s < 3); two producer warps arrive
-  BKE0 = 4,      // K stage s free again (Q K^T done)
-  BV0 = 7,       // V stage s landed (s < 2); two producer warps arrive
-  BVE0 = 9,      // V stage s free again (P V done)
-  BS0 = 11,      // S buffer s holds Q K^T of the current tile
-  BP = 13,       // P of the current tile written (128 softmax threads)
-  BPV = 14,      // P V of the current tile accumulated into O
-  BDRAIN = 15,   // all MMAs of the CTA finished
+  BK0 = 1,       // K of stage s landed (BK0 + s, s < 3); two producer warps arrive
+  BV0 = 4,       // V of stage s landed; two producer warps arrive
+  BE0 = 7,       // stage s free again: P V of its tile done (one commit per tile)
+  BS0 = 10,      // S buffer s holds Q K^T of tile t (s = t & 1)
+  BP0 = 12,      // P of tile t written (BP0 + (t & 1); 128 softmax threads)
+  BDRAIN = 14,   // all MMAs of the CTA finished
+  BQT = 15,      // Q copied into TMEM (128 softmax threads)
   BFULL0 = 16,   // decode ring stage landed (16 .. 16+kMaxDecStages-1)
   BEMPTY0 = BFULL0 + kMaxDecStages,  // decode ring stage free
   kNumBars = BEMPTY0 + kMaxDecStages
@@ -187,7 +184,6 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
   const int kv0 = it.kv_begin, kv1 = it.kv_end;
   const int ntiles = (kv1 - kv0 + kKvTile - 1) / kKvTile;
   const uint32_t sQ = base + C::kOffQ;
-  const uint32_t sP = base + C::kOffP;
   auto sK = [&](int s) { return base + C::kOffK + static_cast<uint32_t>(s * C::kKvBytes); };
   auto sV = [&](int s) { return base + C::kOffV + static_cast<uint32_t>(s * C::kKvBytes); };
   constexpr int kPages = kKvTile / kPageSize;  // 8 pages per tile
@@ -210,8 +206,8 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     const int pg0 = (pr & 1) * (kPages / 2);
     const CUtensorMap* tm = isK ? tm_k : tm_v;
     const uint64_t pol = ptx::policy_evict_last();  // other q tiles re-read these K/V
-    const int NS = isK ? C::kKStages : C::kVStages;
-    const int full0 = isK ? BK0 : BV0, empty0 = isK ? BKE0 : BVE0;
+    const int NS = C::kKStages;
+    const int full0 = isK ? BK0 : BV0, empty0 = BE0;
     int t = 0;
     for (; t < ntiles; ++t) {
       const int s = t % NS;
@@ -247,6 +243,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     constexpr uint32_t kIdPV = ptx::idesc_bf16(128, D, true);
     const uint32_t tS = tmem;        // S buffers: columns [0,128) and [128,256)
     const uint32_t tO = tmem + 256;  // O: columns [256, 256 + D)
+    const uint32_t tQ = tmem + 384;  // Q: columns [384, 384 + D/2), two bf16 per column
     bool issued = false;
     auto qk = [&](int t) -> bool {
       const int s = t % C::kKStages;
@@ -254,25 +251,30 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       ptx::tc_fence_after();
       if (lane == 0) {
 #pragma unroll
+        // A = Q from TMEM (loaded once per item), B = the K tile from shared memory
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-          ptx::mma_ss(tS + (t & 1) * kKvTile, ptx::sdesc_sw128(sQ + off, 16, 1024),
-                      ptx::sdesc_sw128(sK(s) + off, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+          ptx::mma_ts(tS + (t & 1) * kKvTile, tQ + kk * 8, ptx::sdesc_sw128(sK(s) + off, 16, 1024),
+                      kIdQK, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(c.b(BS0 + (t & 1)));
-        ptx::mma_commit(c.b(BKE0 + s));
       }
       __syncwarp();
       issued = true;
       return true;
     };
-    bool ok = wait_on(c, c.b(BQ), 0);
+    bool ok = wait_on(c, c.b(BQT), 0);
     if (ok) ok = qk(0);
     for (int t = 0; ok && t < ntiles; ++t) {
       if (t + 1 < ntiles && !(ok = qk(t + 1))) break;
-      if (!(ok = wait_on(c, c.b(BP), t & 1))) break;
+      // P(t) barriers alternate with the tile parity, like the S buffers: a
+      // barrier is reused by tile t + 2 only after this warp passed tile t, so
+      // no waiter can fall two phases behind
+      if (!(ok = wait_on(c, c.b(BP0 + (t & 1)), (t >> 1) & 1))) break;
       const int s = t % C::kVStages;
       if (!(ok = wait_on(c, c.b(BV0 + s), (t / C::kVStages) & 1))) break;
+      // (every tcgen05.commit costs the tensor pipe a bubble of ~160 cycles, so
+      // a tile commits twice: S ready after Q K^T, stage free after P V)
       const int nval = kv1 - (kv0 + t * kKvTile);
       if (nval < kKvTile && (nval & (kPageSize - 1))) {
         // Rows past the item's last key inside its last page may be unused
@@ -292,15 +294,14 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       }
       ptx::tc_fence_after();
       if (lane == 0) {
+        // P (bf16, two keys per 32-bit column) sits in the first 64 columns of S buffer t & 1
 #pragma unroll
         for (int kk = 0; kk < kKvTile / 16; ++kk) {
-          ptx::mma_ss(tO,
-                      ptx::sdesc_sw128(sP + (kk >> 2) * C::kHalfBytes + (kk & 3) * 32, 16, 1024),
+          ptx::mma_ts(tO, tS + (t & 1) * kKvTile + kk * 8,
                       ptx::sdesc_sw128(sV(s) + kk * 16 * 128, C::kHalfBytes, 1024), kIdPV,
                       (t > 0 || kk > 0) ? 1u : 0u);
         }
-        ptx::mma_commit(c.b(BPV));
-        ptx::mma_commit(c.b(BVE0 + s));
+        ptx::mma_commit(c.b(BE0 + s));
       }
       __syncwarp();
     }
@@ -324,10 +325,31 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     int jmax = sg.hist + tok_c;
     jmax = jmax < kv1 - 1 ? jmax : kv1 - 1;
     const float sl2 = p.scale_log2;
-    uint8_t* gP = gb + C::kOffP;
     float m_ref = neg_inf(), l = 0.f;
-    bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
+    bool ok = wait_on(c, c.b(BQ), 0);
+    {
+      // Q is read for every KV tile: move this thread's row from the swizzled
+      // shared-memory tile into TMEM (K-major, two bf16 per column) once, so
+      // Q K^T runs with A in TMEM and only K read from shared memory.
+      uint32_t qv[D / 2];
+      const uint8_t* qrow = gb + C::kOffQ + row * 128;
+#pragma unroll
+      for (int h = 0; h < C::kHalves; ++h)
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 v = *reinterpret_cast<const uint4*>(qrow + h * C::kHalfBytes + ((ch ^ (row & 7)) << 4));
+          qv[h * 32 + ch * 4 + 0] = v.x;
+          qv[h * 32 + ch * 4 + 1] = v.y;
+          qv[h * 32 + ch * 4 + 2] = v.z;
+          qv[h * 32 + ch * 4 + 3] = v.w;
+        }
+#pragma unroll
+      for (int j = 0; j < D / 64; ++j) ptx::tmem_st32(tmem + 384 + lane_base + j * 32, qv + j * 32);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.b(BQT));
+    }
+    for (int t = 0; ok && t < ntiles; ++t) {
       const int s = t & 1;
       if (!(ok = wait_on(c, c.b(BS0 + s), (t >> 1) & 1))) break;
       ptx::tc_fence_after();
@@ -336,18 +358,24 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       for (int j = 0; j < kKvTile / 32; ++j) ptx::tmem_ld32(tS + s * kKvTile + j * 32, r + j * 32);
       ptx::tmem_wait_ld();
       const int key0 = kv0 + t * kKvTile;
-      float mx = neg_inf();  // max of the raw scores (sm_scale > 0 keeps the order)
+      // max of the raw scores (sm_scale > 0 keeps the order), eight independent chains
+      float mxp[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mxp[j] = neg_inf();
       if (key0 + kKvTile - 1 <= jmax) {  // every key of the tile is visible to this row
 #pragma unroll
-        for (int i = 0; i < kKvTile; ++i) mx = fmaxf(mx, __uint_as_float(r[i]));
+        for (int i = 0; i < kKvTile; i += 2)
+          mxp[(i >> 1) & 7] = ptx::max3(mxp[(i >> 1) & 7], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
       } else {  // diagonal / last tile: mask keys past this row's last visible key
 #pragma unroll
         for (int i = 0; i < kKvTile; ++i) {
           const float x = (key0 + i <= jmax) ? __uint_as_float(r[i]) : neg_inf();
           r[i] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          mxp[i & 7] = fmaxf(mxp[i & 7], x);
         }
       }
+      const float mx = ptx::max3(ptx::max3(mxp[0], mxp[1], mxp[2]), ptx::max3(mxp[3], mxp[4], mxp[5]),
+                                 fmaxf(mxp[6], mxp[7]));
       const float m_new = fmaxf(m_ref, mx * sl2);
       const bool rescale = m_new > m_ref + kRescaleThreshold;
       float alpha = 1.f;
@@ -356,48 +384,52 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
         m_ref = m_new;
       }
       const float neg_m = m_ref == neg_inf() ? 0.f : -m_ref;
-      float sum = 0.f;
-      // bf16 pairs of P overwrite the consumed scores in place: r[i/2] after r[i], r[i+1]
+      // P = 2^(s * scale_log2 - m).  bf16 pairs of P overwrite the consumed
+      // scores in place: r[i/2] after r[i], r[i+1]; the row sum runs in eight
+      // independent chains.
+      float sp[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sp[j] = 0.f;
 #pragma unroll
       for (int i = 0; i < kKvTile; i += 2) {
-        const float p0 = ptx::ex2(fmaf(__uint_as_float(r[i]), sl2, neg_m));
-        const float p1 = ptx::ex2(fmaf(__uint_as_float(r[i + 1]), sl2, neg_m));
-        sum += p0 + p1;
+        const float x0 = fmaf(__uint_as_float(r[i]), sl2, neg_m);
+        const float x1 = fmaf(__uint_as_float(r[i + 1]), sl2, neg_m);
+        const float p0 = ptx::ex2(x0);
+        const float p1 = ptx::ex2(x1);
+        sp[(i >> 1) & 7] += p0 + p1;
         r[i / 2] = ptx::pack_bf16x2(p0, p1);
       }
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l = l * alpha + sum;
-      if (t > 0) {
-        // P V of the previous tile must be done before O is rescaled and P overwritten
-        if (!(ok = wait_on(c, c.b(BPV), (t - 1) & 1))) break;
+      // P(t) goes to the first 64 columns of S buffer t & 1 (this thread's lane,
+      // already read); P V(t-1) reads the other buffer, so no wait is needed here
+      ptx::tmem_st32(tS + s * kKvTile, r);
+      ptx::tmem_st32(tS + s * kKvTile + 32, r + 32);
+      if (t > 0 && __any_sync(0xffffffffu, rescale)) {
+        // P V of the previous tile must be done before O is rescaled: it frees
+        // stage (t-1) % 3.  That barrier is at most one phase off: its next use
+        // needs P(t+2), and S(t) ready implies every earlier MMA is complete.
+        const int ps = (t - 1) % C::kKStages;
+        if (!(ok = wait_on(c, c.b(BE0 + ps), ((t - 1) / C::kKStages) & 1))) break;
         ptx::tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-          for (int j = 0; j < D / 32; ++j) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + j * 32, o);
-            ptx::tmem_wait_ld();
-            if (rescale) {
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + j * 32, o);
+          ptx::tmem_wait_ld();
+          if (rescale) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            }
-            ptx::tmem_st32(tO + j * 32, o);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           }
-          ptx::tmem_wait_st();
+          ptx::tmem_st32(tO + j * 32, o);
         }
       }
-      // P row -> shared memory, K-major with the 128-byte swizzle: keys
-      // [64h, 64h + 64) of this row in panel h, 16-byte chunk j at j ^ (row & 7)
-#pragma unroll
-      for (int ch = 0; ch < kKvTile / 8; ++ch) {
-        const int h = ch >> 3, cc = ch & 7;
-        *reinterpret_cast<uint4*>(gP + h * C::kHalfBytes + row * 128 + ((cc ^ (row & 7)) << 4)) =
-            make_uint4(r[ch * 4], r[ch * 4 + 1], r[ch * 4 + 2], r[ch * 4 + 3]);
-      }
-      ptx::fence_proxy_async_smem();
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(c.b(BP));
+      ptx::mbar_arrive(c.b(BP0 + (t & 1)));
     }
-    if (ok && ntiles > 0) ok = wait_on(c, c.b(BPV), (ntiles - 1) & 1);
+    // every MMA of the item (the MMA warp commits this once, after the last P V)
+    if (ok && ntiles > 0) ok = wait_on(c, c.b(BDRAIN), 0);
     ptx::tc_fence_after();
     const bool store = ok && valid && !*c.abort;
     const bool direct = it.part_row < 0;
@@ -759,8 +791,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;
-      if ((i >= BK0 && i < BK0 + 3) || (i >= BV0 && i < BV0 + 2)) count = 2;  // two producer warps
-      if (i == BP) count = 128;                        // every softmax thread
+      if (i >= BK0 && i < BV0 + 3) count = 2;          // two producer warps per K / V tile
+      if (i == BP0 || i == BP0 + 1 || i == BQT) count = 128;  // every softmax thread
       if (i >= BEMPTY0) count = prefill ? 1 : it.num_heads;  // one warp per head reads a stage
       ptx::mbar_init(c.b(i), count);
     }
