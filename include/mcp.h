@@ -156,7 +156,8 @@ typedef struct mcp_plan {
   int64_t off_items, off_combine, off_part_o, off_part_lse, off_error;
   int64_t workspace_bytes;    /* bytes the workspace must have                   */
   mcp_attn_desc desc;         /* the description the plan was built for          */
-  int32_t reserved[8];
+  int32_t combine_rows;       /* query rows (token, head) merged by the combine  */
+  int32_t reserved[7];
 } mcp_plan;
 
 /*

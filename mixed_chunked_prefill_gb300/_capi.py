@@ -63,7 +63,8 @@ class Plan(ctypes.Structure):
         ("off_error", c_int64),
         ("workspace_bytes", c_int64),
         ("desc", AttnDesc),
-        ("reserved", c_int32 * 8),
+        ("combine_rows", c_int32),
+        ("reserved", c_int32 * 7),
     ]
 
 

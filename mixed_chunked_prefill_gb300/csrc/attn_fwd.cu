@@ -200,7 +200,11 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     drain_wait(c.abort, c.err, c.b(BQ), 0);
   } else if (warp >= 6) {
     // -------------------------------------- K/V producers: four warps
-    // warp 6: K pages 0-3, warp 7: K pages 4-7, warp 8: V pages 0-3, warp 9: V pages 4-7
+    // warp 6: K pages 0-3, warp 7: K pages 4-7, warp 8: V pages 0-3, warp 9: V pages 4-7.
+    // A K tile arrives as one box per (page, 64-column panel) so that each
+    // panel holds 128 consecutive keys (the K-major operand of Q K^T); a V tile
+    // arrives as one box per page, [panel][16 tokens][128 B], which P V reads
+    // one page (16 keys) per MMA.
     const int pr = warp - 6;
     const bool isK = pr < 2;
     const int pg0 = (pr & 1) * (kPages / 2);
@@ -208,27 +212,42 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     const uint64_t pol = ptx::policy_evict_last();  // other q tiles re-read these K/V
     const int NS = C::kKStages;
     const int full0 = isK ? BK0 : BV0, empty0 = BE0;
+    // the block-table entries of tile t + 1 are read while tile t is issued, so
+    // that the dependent global load is off the stage-refill path
+    auto fetch = [&](int tt) -> int {
+      const int key0 = kv0 + tt * kKvTile;
+      const int npg = (kv1 - key0 + kPageSize - 1) / kPageSize;  // pages of the tile inside the item
+      const bool mine = lane < kPages / 2 && pg0 + lane < npg;
+      return mine ? page_of(p, it.seg, key0 / kPageSize + pg0 + lane) : p.num_pages;
+    };
+    int pg_next = ntiles > 0 ? fetch(0) : p.num_pages;
     int t = 0;
     for (; t < ntiles; ++t) {
       const int s = t % NS;
+      const int pg = pg_next;
+      if (t + 1 < ntiles) pg_next = fetch(t + 1);
       if (t >= NS && !wait_on(c, c.b(empty0 + s), ((t / NS) + 1) & 1)) break;
-      const int key0 = kv0 + t * kKvTile;
-      int npg = (kv1 - key0 + kPageSize - 1) / kPageSize;  // pages of the tile inside the item
-      const int mine = lane < kPages / 2 && pg0 + lane < npg;
-      const int pg = mine ? page_of(p, it.seg, key0 / kPageSize + pg0 + lane) : p.num_pages;
       int pgs[kPages / 2];
 #pragma unroll
       for (int i = 0; i < kPages / 2; ++i) pgs[i] = __shfl_sync(0xffffffffu, pg, i);
       if (lane == 0) {
         const uint32_t bar = c.b(full0 + s);
-        const uint32_t dst = isK ? sK(s) : sV(s);
         ptx::mbar_arrive_expect_tx(bar, C::kKvBytes / 2);
+        if (isK) {
+          const uint32_t dst = sK(s);
 #pragma unroll
-        for (int i = 0; i < kPages / 2; ++i)
+          for (int i = 0; i < kPages / 2; ++i)
 #pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
-            ptx::tma_load_5d(dst + h * C::kHalfBytes + (pg0 + i) * kPageSize * 128, tm, bar, 0, h,
-                             it.kv_head, 0, pgs[i], pol);
+            for (int h = 0; h < C::kHalves; ++h)
+              ptx::tma_load_5d(dst + h * C::kHalfBytes + (pg0 + i) * kPageSize * 128, tm, bar, 0,
+                               h, it.kv_head, 0, pgs[i], pol);
+        } else {
+          const uint32_t dst = sV(s);
+#pragma unroll
+          for (int i = 0; i < kPages / 2; ++i)
+            ptx::tma_load_5d(dst + (pg0 + i) * C::kHeadBlock, tm, bar, 0, 0, 0, it.kv_head, pgs[i],
+                             pol);
+        }
       }
       __syncwarp();
     }
@@ -244,18 +263,26 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     const uint32_t tS = tmem;        // S buffers: columns [0,128) and [128,256)
     const uint32_t tO = tmem + 256;  // O: columns [256, 256 + D)
     const uint32_t tQ = tmem + 384;  // Q: columns [384, 384 + D/2), two bf16 per column
+    // Descriptors of stage 0, built once: an MMA then only adds a byte offset >> 4
+    // to the start-address field (shared addresses stay below 256 KB, so the
+    // add never carries out of that field).  Rebuilding the descriptor per MMA
+    // made the single issuing thread, not the tensor pipe, set the MMA rate.
+    const uint64_t dK0 = ptx::sdesc_sw128(sK(0), 16, 1024);
+    const uint64_t dV0 = ptx::sdesc_sw128(sV(0), kPageSize * 128, 1024);
     bool issued = false;
     auto qk = [&](int t) -> bool {
       const int s = t % C::kKStages;
       if (!wait_on(c, c.b(BK0 + s), (t / C::kKStages) & 1)) return false;
       ptx::tc_fence_after();
       if (lane == 0) {
-#pragma unroll
+        const uint64_t dk = dK0 + static_cast<uint64_t>((s * C::kKvBytes) >> 4);
+        const uint32_t ts = tS + (t & 1) * kKvTile;
         // A = Q from TMEM (loaded once per item), B = the K tile from shared memory
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-          ptx::mma_ts(tS + (t & 1) * kKvTile, tQ + kk * 8, ptx::sdesc_sw128(sK(s) + off, 16, 1024),
-                      kIdQK, kk > 0 ? 1u : 0u);
+          constexpr int kPanel = C::kHalfBytes;
+          ptx::mma_ts(ts, tQ + kk * 8, dk + (((kk >> 2) * kPanel + (kk & 3) * 32) >> 4), kIdQK,
+                      kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(c.b(BS0 + (t & 1)));
       }
@@ -273,8 +300,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       if (!(ok = wait_on(c, c.b(BP0 + (t & 1)), (t >> 1) & 1))) break;
       const int s = t % C::kVStages;
       if (!(ok = wait_on(c, c.b(BV0 + s), (t / C::kVStages) & 1))) break;
-      // (every tcgen05.commit costs the tensor pipe a bubble of ~160 cycles, so
-      // a tile commits twice: S ready after Q K^T, stage free after P V)
+      // a tile commits twice: S ready after Q K^T, stage free after P V
       const int nval = kv1 - (kv0 + t * kKvTile);
       if (nval < kKvTile && (nval & (kPageSize - 1))) {
         // Rows past the item's last key inside its last page may be unused
@@ -286,21 +312,22 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
         for (int i = lane; i < per_half * C::kHalves; i += 32) {
           const int h = i / per_half, rem = i - h * per_half;
           const int r = r0 + rem / 8, ch = rem & 7;
-          *reinterpret_cast<uint4*>(gV + h * C::kHalfBytes + r * 128 + ch * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(gV + (r / kPageSize) * C::kHeadBlock + h * kPageSize * 128 +
+                                    (r % kPageSize) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
       }
       ptx::tc_fence_after();
       if (lane == 0) {
-        // P (bf16, two keys per 32-bit column) sits in the first 64 columns of S buffer t & 1
+        const uint64_t dv = dV0 + static_cast<uint64_t>((s * C::kKvBytes) >> 4);
+        const uint32_t tp = tS + (t & 1) * kKvTile;
+        // P (bf16, two keys per 32-bit column) sits in the first 64 columns of S
+        // buffer t & 1; MMA kk takes the 16 keys of page kk of the V tile
+        ptx::mma_ts(tO, tp, dv, kIdPV, t > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kKvTile / 16; ++kk) {
-          ptx::mma_ts(tO, tS + (t & 1) * kKvTile + kk * 8,
-                      ptx::sdesc_sw128(sV(s) + kk * 16 * 128, C::kHalfBytes, 1024), kIdPV,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < kKvTile / 16; ++kk)
+          ptx::mma_ts(tO, tp + kk * 8, dv + ((kk * C::kHeadBlock) >> 4), kIdPV, 1u);
         ptx::mma_commit(c.b(BE0 + s));
       }
       __syncwarp();
@@ -907,6 +934,15 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
                              (cuuint64_t)a.page_size * a.num_kv_heads * D * 2};
     cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)a.page_size, 1};
     if (!encode(&tk, a.k_cache, 5, dims, strides, box, "k_cache")) return -1;
+  }
+  {
+    // a whole page of one kv head: dims {d, token, panel, head, page}, so that
+    // shared memory receives [panel][token][64]
+    cuuint64_t dims[5] = {64, (cuuint64_t)a.page_size, (cuuint64_t)(D / 64),
+                          (cuuint64_t)a.num_kv_heads, (cuuint64_t)a.num_pages};
+    cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * D * 2, 128, (cuuint64_t)D * 2,
+                             (cuuint64_t)a.page_size * a.num_kv_heads * D * 2};
+    cuuint32_t box[5] = {64, (cuuint32_t)a.page_size, (cuuint32_t)(D / 64), 1, 1};
     if (!encode(&tv, a.v_cache, 5, dims, strides, box, "v_cache")) return -1;
   }
   {

@@ -20,44 +20,90 @@ constexpr float kLog2e = 1.44269504088896341f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-// One CTA per combine entry, one warp per row; lane l holds D/32 columns.
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One warp per merged row.  The rows of all entries are numbered
+// consecutively (entry e owns rows [row_base, row_base + rows)), so the grid
+// covers exactly the rows that have parts, whatever the mix of short decode
+// entries and 128-row chunk tiles.  Lane k holds the LSE of part k (32 parts
+// per pass); lane l accumulates columns [l * D/32, (l + 1) * D/32) of O.
 template <int D>
-__global__ void __launch_bounds__(128) combine_kernel(const CombineEntry* __restrict__ ents,
+__global__ void __launch_bounds__(256) combine_kernel(const CombineEntry* __restrict__ ents,
+                                                      int num_ents, int total_rows,
                                                       const int32_t* __restrict__ cu_q,
                                                       const float* __restrict__ part_o,
                                                       const float* __restrict__ part_lse,
                                                       __nv_bfloat16* __restrict__ out,
                                                       float* __restrict__ lse, int hq, int G) {
   constexpr int V = D / 32;
-  const CombineEntry e = ents[blockIdx.x];
-  const int q_start = cu_q[e.seg];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int row = warp; row < e.rows; row += blockDim.x / 32) {
-    float M = neg_inf();
-    for (int k = 0; k < e.num_splits; ++k)
-      M = fmaxf(M, part_lse[e.part_row + static_cast<int64_t>(k) * e.rows + row]);
-    float acc[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] = 0.f;
-    float L = 0.f;
-    for (int k = 0; k < e.num_splits; ++k) {
-      const int64_t pr = e.part_row + static_cast<int64_t>(k) * e.rows + row;
-      const float lk = part_lse[pr];
-      const float w = (lk == neg_inf()) ? 0.f : ptx::ex2((lk - M) * kLog2e);
-      L += w;
-      const float* src = part_o + pr * D + lane * V;
-#pragma unroll
-      for (int v = 0; v < V; ++v) acc[v] += w * src[v];
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int tok = e.q_begin + row / G;
-    const int g = row - (row / G) * G;
-    const int64_t orow = static_cast<int64_t>(q_start + tok) * hq + e.kv_head * G + g;
-    uint32_t* dst = reinterpret_cast<uint32_t*>(out + orow * D + lane * V);
-#pragma unroll
-    for (int v = 0; v < V; v += 2) dst[v / 2] = ptx::pack_bf16x2(acc[v] * inv, acc[v + 1] * inv);
-    if (lse && lane == 0) lse[orow] = L > 0.f ? M + logf(L) : neg_inf();
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= total_rows) return;
+  const int lane = threadIdx.x & 31;
+  // the entry holding flat row r: the last one with row_base <= r
+  int lo = 0, hi = num_ents - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(&ents[mid].row_base) <= r) lo = mid;
+    else hi = mid - 1;
   }
+  const CombineEntry e = ents[lo];
+  const int row = r - e.row_base;
+  const int n = e.num_splits;
+  const int64_t pr0 = static_cast<int64_t>(e.part_row) + row;  // part k: row pr0 + k * e.rows
+
+  float M = neg_inf();
+  for (int k = lane; k < n; k += 32) M = fmaxf(M, part_lse[pr0 + static_cast<int64_t>(k) * e.rows]);
+  M = warp_max(M);
+
+  float acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+  float L = 0.f;
+  for (int k0 = 0; k0 < n; k0 += 32) {
+    const int k = k0 + lane;
+    const float lk = k < n ? part_lse[pr0 + static_cast<int64_t>(k) * e.rows] : neg_inf();
+    const float w = (lk == neg_inf()) ? 0.f : ptx::ex2((lk - M) * kLog2e);
+    L += w;
+    const int cnt = n - k0 < 32 ? n - k0 : 32;
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      const float* src = part_o + (pr0 + static_cast<int64_t>(k0 + j) * e.rows) * D + lane * V;
+      if constexpr (V == 4) {
+        const float4 o = __ldg(reinterpret_cast<const float4*>(src));
+        acc[0] += wj * o.x;
+        acc[1] += wj * o.y;
+        acc[2] += wj * o.z;
+        acc[3] += wj * o.w;
+      } else {
+        const float2 o = __ldg(reinterpret_cast<const float2*>(src));
+        acc[0] += wj * o.x;
+        acc[1] += wj * o.y;
+      }
+    }
+  }
+  L = warp_sum(L);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int tok = e.q_begin + row / G;
+  const int g = row - (row / G) * G;
+  const int64_t orow = static_cast<int64_t>(cu_q[e.seg] + tok) * hq + e.kv_head * G + g;
+  if constexpr (V == 4) {
+    uint2* dst = reinterpret_cast<uint2*>(out + orow * D + lane * V);
+    *dst = make_uint2(ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                      ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(out + orow * D + lane * V) = ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+  if (lse && lane == 0) lse[orow] = L > 0.f ? M + logf(L) : neg_inf();
 }
 
 // Standalone merge: one warp per (row, head); o_parts [n, rows, heads, D].
@@ -93,17 +139,18 @@ __global__ void __launch_bounds__(128) merge_states_kernel(const float* __restri
 }  // namespace
 
 int launch_combine(const FwdArgs& a, void* stream) {
-  if (a.num_combine <= 0) return 0;
+  if (a.num_combine <= 0 || a.combine_rows <= 0) return 0;
   const int G = a.num_q_heads / a.num_kv_heads;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int blocks = (a.combine_rows + 7) / 8;
   if (a.head_dim == 128) {
-    combine_kernel<128><<<a.num_combine, 128, 0, st>>>(
-        a.combine, a.cu_seqlens_q, a.part_o, a.part_lse, static_cast<__nv_bfloat16*>(a.out), a.lse,
-        a.num_q_heads, G);
+    combine_kernel<128><<<blocks, 256, 0, st>>>(
+        a.combine, a.num_combine, a.combine_rows, a.cu_seqlens_q, a.part_o, a.part_lse,
+        static_cast<__nv_bfloat16*>(a.out), a.lse, a.num_q_heads, G);
   } else {
-    combine_kernel<64><<<a.num_combine, 128, 0, st>>>(
-        a.combine, a.cu_seqlens_q, a.part_o, a.part_lse, static_cast<__nv_bfloat16*>(a.out), a.lse,
-        a.num_q_heads, G);
+    combine_kernel<64><<<blocks, 256, 0, st>>>(
+        a.combine, a.num_combine, a.combine_rows, a.cu_seqlens_q, a.part_o, a.part_lse,
+        static_cast<__nv_bfloat16*>(a.out), a.lse, a.num_q_heads, G);
   }
   return static_cast<int>(cudaGetLastError());
 }

@@ -429,6 +429,12 @@ mcp_status plan_common(const mcp_attn_desc* desc, const int32_t* cu, const int32
   pl.num_decode_items = b.n_dec;
   pl.num_prefill_items = b.n_pre;
   pl.num_combine = static_cast<int32_t>(b.comb.size());
+  int64_t crow = 0;
+  for (mcp::CombineEntry& e : b.comb) {
+    e.row_base = static_cast<int32_t>(crow);
+    crow += e.rows;
+  }
+  pl.combine_rows = static_cast<int32_t>(crow);
   pl.decode_split_tokens = b.dsplit;
   pl.prefill_split_tokens = b.psplit;
   pl.num_sms = num_sms;
@@ -541,6 +547,7 @@ mcp_status mcp_mixed_attn_fwd(const mcp_plan* plan, const void* q, const void* k
   a.error_word = reinterpret_cast<int32_t*>(ws + plan->off_error);
   a.num_items = plan->num_items;
   a.num_combine = plan->num_combine;
+  a.combine_rows = plan->combine_rows;
   a.total_q = d.total_q;
   a.num_q_heads = d.num_q_heads;
   a.num_kv_heads = d.num_kv_heads;

@@ -48,7 +48,7 @@ struct CombineEntry {
   int32_t num_splits;
   int32_t part_row;
   int32_t rows;      // q_count * G
-  int32_t pad;
+  int32_t row_base;  // rows of all entries are numbered consecutively: this entry's first
 };
 static_assert(sizeof(CombineEntry) == 32, "CombineEntry layout");
 
@@ -68,6 +68,7 @@ struct FwdArgs {
   int32_t* error_word;
   int32_t num_items;
   int32_t num_combine;
+  int32_t combine_rows;
   int32_t total_q;
   int32_t num_q_heads;
   int32_t num_kv_heads;

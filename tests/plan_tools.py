@@ -13,7 +13,7 @@ ITEM = np.dtype([("seg", "<i4"), ("kv_head", "<i2"), ("kind", "i1"), ("num_heads
                  ("q_begin", "<i4"), ("q_count", "<i4"), ("kv_begin", "<i4"), ("kv_end", "<i4"),
                  ("part_row", "<i4"), ("part_head_stride", "<i4")])
 COMB = np.dtype([("seg", "<i4"), ("kv_head", "<i4"), ("q_begin", "<i4"), ("q_count", "<i4"),
-                 ("num_splits", "<i4"), ("part_row", "<i4"), ("rows", "<i4"), ("pad", "<i4")])
+                 ("num_splits", "<i4"), ("part_row", "<i4"), ("rows", "<i4"), ("row_base", "<i4")])
 
 
 def desc_for(w):

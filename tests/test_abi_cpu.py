@@ -258,6 +258,11 @@ def check_plan_covers(w, items, comb, plan):
         assert parts == [int(e["part_row"]) + k * int(e["rows"]) for k in range(len(ranges))]
         used[e["part_row"]:e["part_row"] + e["num_splits"] * e["rows"]] += 1
     assert (used <= 1).all()
+    # the combine kernel's flat row numbering: entries own consecutive row ranges
+    if len(comb):
+        starts = np.concatenate([[0], np.cumsum(comb["rows"])[:-1]])
+        assert np.array_equal(comb["row_base"], starts)
+    assert plan.combine_rows == int(comb["rows"].sum()) if len(comb) else plan.combine_rows == 0
 
 
 @pytest.mark.parametrize("name", synth.CONFIG_NAMES)
