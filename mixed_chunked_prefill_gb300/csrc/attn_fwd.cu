@@ -81,12 +81,13 @@ enum : int {
   BQ = 0,        // Q tile landed
   BK0 = 1,       // K of stage s landed (BK0 + s, s < 3); two producer warps arrive
   BV0 = 4,       // V of stage s landed; two producer warps arrive
-  BE0 = 7,       // stage s free again: P V of its tile done (one commit per tile)
+  BE0 = 7,       // P V of the tile in stage s done: V stage free, O updated
   BS0 = 10,      // S buffer s holds Q K^T of tile t (s = t & 1)
   BP0 = 12,      // P of tile t written (BP0 + (t & 1); 128 softmax threads)
-  BDRAIN = 14,   // all MMAs of the CTA finished
+  BDRAIN = 14,   // all MMAs of the CTA finished (both issuing warps commit)
   BQT = 15,      // Q copied into TMEM (128 softmax threads)
-  BFULL0 = 16,   // decode ring stage landed (16 .. 16+kMaxDecStages-1)
+  BKE0 = 16,     // Q K^T of the tile in stage s done: K stage free
+  BFULL0 = 19,   // decode ring stage landed (BFULL0 .. BFULL0+kMaxDecStages-1)
   BEMPTY0 = BFULL0 + kMaxDecStages,  // decode ring stage free
   kNumBars = BEMPTY0 + kMaxDecStages
 };
@@ -188,8 +189,15 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
   auto sV = [&](int s) { return base + C::kOffV + static_cast<uint32_t>(s * C::kKvBytes); };
   constexpr int kPages = kKvTile / kPageSize;  // 8 pages per tile
 
+  // Two warps issue the MMAs: warp 1 Q K^T, warp 0 P V.  Each waits only for
+  // its own operands, so one warp's barrier waits overlap the other's MMAs
+  // (with a single issuer the waits sat between every pair of MMA groups and
+  // the tensor pipe idled for them).  Both feed the same in-order tensor pipe;
+  // Q K^T(t) waits for P V(t - 2), the last reader of S buffer t & 1.
+  constexpr uint32_t kIdQK = ptx::idesc_bf16(128, kKvTile, false);
+  constexpr uint32_t kIdPV = ptx::idesc_bf16(128, D, true);
   if (warp == 0) {
-    // ------------------------------------------------------ Q tile (TMA)
+    // ---------------------------------------- Q tile (TMA), then P V issuer
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(c.b(BQ), C::kHalves * G * TQ * 128);
       for (int h = 0; h < C::kHalves; ++h)
@@ -197,6 +205,53 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
                          sg.q_start + it.q_begin, ptx::policy_evict_first());
     }
     __syncwarp();
+    const uint32_t tS = tmem;        // S buffers: columns [0,128) and [128,256)
+    const uint32_t tO = tmem + 256;  // O: columns [256, 256 + D)
+    // descriptor of stage 0 built once; an MMA adds a byte offset >> 4 to the
+    // start-address field (shared addresses stay below 256 KB: no carry out)
+    const uint64_t dV0 = ptx::sdesc_sw128(sV(0), kPageSize * 128, 1024);
+    bool ok = true;
+    for (int t = 0; ok && t < ntiles; ++t) {
+      // P(t) barriers alternate with the tile parity, like the S buffers: the
+      // barrier is reused by tile t + 2 only after Q K^T(t + 2), which waits
+      // for this P V(t), so no waiter falls two phases behind
+      if (!(ok = wait_on(c, c.b(BP0 + (t & 1)), (t >> 1) & 1))) break;
+      const int s = t % C::kVStages;
+      if (!(ok = wait_on(c, c.b(BV0 + s), (t / C::kVStages) & 1))) break;
+      const int nval = kv1 - (kv0 + t * kKvTile);
+      if (nval < kKvTile && (nval & (kPageSize - 1))) {
+        // Rows past the item's last key inside its last page may be unused
+        // cache slots holding anything (NaN included); P is 0 there but
+        // 0 * NaN would reach O, so those V rows are zeroed.
+        const int r0 = nval, nr = ((nval + kPageSize - 1) & ~(kPageSize - 1)) - nval;
+        const int per_half = nr * 8;
+        uint8_t* gV = gb + (sV(s) - base);
+        for (int i = lane; i < per_half * C::kHalves; i += 32) {
+          const int h = i / per_half, rem = i - h * per_half;
+          const int r = r0 + rem / 8, ch = rem & 7;
+          *reinterpret_cast<uint4*>(gV + (r / kPageSize) * C::kHeadBlock + h * kPageSize * 128 +
+                                    (r % kPageSize) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+      }
+      ptx::tc_fence_after();
+      if (lane == 0) {
+        const uint64_t dv = dV0 + static_cast<uint64_t>((s * C::kKvBytes) >> 4);
+        const uint32_t tp = tS + (t & 1) * kKvTile;
+        // P (bf16, two keys per 32-bit column) sits in the first 64 columns of S
+        // buffer t & 1; MMA kk takes the 16 keys of page kk of the V tile
+        ptx::mma_ts(tO, tp, dv, kIdPV, t > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 1; kk < kKvTile / 16; ++kk)
+          ptx::mma_ts(tO, tp + kk * 8, dv + ((kk * C::kHeadBlock) >> 4), kIdPV, 1u);
+        ptx::mma_commit(c.b(BE0 + s));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) ptx::mma_commit(c.b(BDRAIN));  // arrives once this warp's MMAs are done
+    __syncwarp();
+    drain_wait(c.abort, c.err, c.b(BDRAIN), 0);
     drain_wait(c.abort, c.err, c.b(BQ), 0);
   } else if (warp >= 6) {
     // -------------------------------------- K/V producers: four warps
@@ -211,7 +266,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     const CUtensorMap* tm = isK ? tm_k : tm_v;
     const uint64_t pol = ptx::policy_evict_last();  // other q tiles re-read these K/V
     const int NS = C::kKStages;
-    const int full0 = isK ? BK0 : BV0, empty0 = BE0;
+    const int full0 = isK ? BK0 : BV0, empty0 = isK ? BKE0 : BE0;
     // the block-table entries of tile t + 1 are read while tile t is issued, so
     // that the dependent global load is off the stage-refill path
     auto fetch = [&](int tt) -> int {
@@ -257,22 +312,19 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       drain_wait(c.abort, c.err, c.b(full0 + s), (last / NS) & 1);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------- MMA issuer
-    constexpr uint32_t kIdQK = ptx::idesc_bf16(128, kKvTile, false);
-    constexpr uint32_t kIdPV = ptx::idesc_bf16(128, D, true);
+    // ------------------------------------------------------ Q K^T issuer
     const uint32_t tS = tmem;        // S buffers: columns [0,128) and [128,256)
-    const uint32_t tO = tmem + 256;  // O: columns [256, 256 + D)
     const uint32_t tQ = tmem + 384;  // Q: columns [384, 384 + D/2), two bf16 per column
-    // Descriptors of stage 0, built once: an MMA then only adds a byte offset >> 4
-    // to the start-address field (shared addresses stay below 256 KB, so the
-    // add never carries out of that field).  Rebuilding the descriptor per MMA
-    // made the single issuing thread, not the tensor pipe, set the MMA rate.
     const uint64_t dK0 = ptx::sdesc_sw128(sK(0), 16, 1024);
-    const uint64_t dV0 = ptx::sdesc_sw128(sV(0), kPageSize * 128, 1024);
-    bool issued = false;
-    auto qk = [&](int t) -> bool {
+    bool ok = wait_on(c, c.b(BQT), 0);
+    for (int t = 0; ok && t < ntiles; ++t) {
       const int s = t % C::kKStages;
-      if (!wait_on(c, c.b(BK0 + s), (t / C::kKStages) & 1)) return false;
+      if (!(ok = wait_on(c, c.b(BK0 + s), (t / C::kKStages) & 1))) break;
+      if (t >= 2) {
+        // S buffer t & 1 still holds P(t - 2) until P V(t - 2) has read it
+        const int ps = (t - 2) % C::kVStages;
+        if (!(ok = wait_on(c, c.b(BE0 + ps), ((t - 2) / C::kVStages) & 1))) break;
+      }
       ptx::tc_fence_after();
       if (lane == 0) {
         const uint64_t dk = dK0 + static_cast<uint64_t>((s * C::kKvBytes) >> 4);
@@ -285,58 +337,13 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
                       kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(c.b(BS0 + (t & 1)));
-      }
-      __syncwarp();
-      issued = true;
-      return true;
-    };
-    bool ok = wait_on(c, c.b(BQT), 0);
-    if (ok) ok = qk(0);
-    for (int t = 0; ok && t < ntiles; ++t) {
-      if (t + 1 < ntiles && !(ok = qk(t + 1))) break;
-      // P(t) barriers alternate with the tile parity, like the S buffers: a
-      // barrier is reused by tile t + 2 only after this warp passed tile t, so
-      // no waiter can fall two phases behind
-      if (!(ok = wait_on(c, c.b(BP0 + (t & 1)), (t >> 1) & 1))) break;
-      const int s = t % C::kVStages;
-      if (!(ok = wait_on(c, c.b(BV0 + s), (t / C::kVStages) & 1))) break;
-      // a tile commits twice: S ready after Q K^T, stage free after P V
-      const int nval = kv1 - (kv0 + t * kKvTile);
-      if (nval < kKvTile && (nval & (kPageSize - 1))) {
-        // Rows past the item's last key inside its last page may be unused
-        // cache slots holding anything (NaN included); P is 0 there but
-        // 0 * NaN would reach O, so those V rows are zeroed.
-        const int r0 = nval, nr = ((nval + kPageSize - 1) & ~(kPageSize - 1)) - nval;
-        const int per_half = nr * 8;
-        uint8_t* gV = gb + (sV(s) - base);
-        for (int i = lane; i < per_half * C::kHalves; i += 32) {
-          const int h = i / per_half, rem = i - h * per_half;
-          const int r = r0 + rem / 8, ch = rem & 7;
-          *reinterpret_cast<uint4*>(gV + (r / kPageSize) * C::kHeadBlock + h * kPageSize * 128 +
-                                    (r % kPageSize) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-      }
-      ptx::tc_fence_after();
-      if (lane == 0) {
-        const uint64_t dv = dV0 + static_cast<uint64_t>((s * C::kKvBytes) >> 4);
-        const uint32_t tp = tS + (t & 1) * kKvTile;
-        // P (bf16, two keys per 32-bit column) sits in the first 64 columns of S
-        // buffer t & 1; MMA kk takes the 16 keys of page kk of the V tile
-        ptx::mma_ts(tO, tp, dv, kIdPV, t > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 1; kk < kKvTile / 16; ++kk)
-          ptx::mma_ts(tO, tp + kk * 8, dv + ((kk * C::kHeadBlock) >> 4), kIdPV, 1u);
-        ptx::mma_commit(c.b(BE0 + s));
+        ptx::mma_commit(c.b(BKE0 + s));
       }
       __syncwarp();
     }
-    if (issued) {
-      if (lane == 0) ptx::mma_commit(c.b(BDRAIN));
-      __syncwarp();
-      drain_wait(c.abort, c.err, c.b(BDRAIN), 0);
-    }
+    if (lane == 0) ptx::mma_commit(c.b(BDRAIN));
+    __syncwarp();
+    drain_wait(c.abort, c.err, c.b(BDRAIN), 0);
   } else {
     // ------------------------------------------- softmax + epilogue (2-5)
     const int qw = warp & 3;
@@ -413,17 +420,18 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       const float neg_m = m_ref == neg_inf() ? 0.f : -m_ref;
       // P = 2^(s * scale_log2 - m).  bf16 pairs of P overwrite the consumed
       // scores in place: r[i/2] after r[i], r[i+1]; the row sum runs in eight
-      // independent chains.
+      // independent chains, two per packed add.
       float sp[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) sp[j] = 0.f;
 #pragma unroll
       for (int i = 0; i < kKvTile; i += 2) {
-        const float x0 = fmaf(__uint_as_float(r[i]), sl2, neg_m);
-        const float x1 = fmaf(__uint_as_float(r[i + 1]), sl2, neg_m);
+        float x0, x1;
+        ptx::fma_f32x2(x0, x1, __uint_as_float(r[i]), __uint_as_float(r[i + 1]), sl2, neg_m);
         const float p0 = ptx::ex2(x0);
         const float p1 = ptx::ex2(x1);
-        sp[(i >> 1) & 7] += p0 + p1;
+        const int j = (i >> 1) & 3;
+        ptx::add_f32x2(sp[2 * j], sp[2 * j + 1], p0, p1);
         r[i / 2] = ptx::pack_bf16x2(p0, p1);
       }
       const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
@@ -820,6 +828,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint32_t count = 1;
       if (i >= BK0 && i < BV0 + 3) count = 2;          // two producer warps per K / V tile
       if (i == BP0 || i == BP0 + 1 || i == BQT) count = 128;  // every softmax thread
+      if (i == BDRAIN) count = 2;                       // the Q K^T and the P V issuer
       if (i >= BEMPTY0) count = prefill ? 1 : it.num_heads;  // one warp per head reads a stage
       ptx::mbar_init(c.b(i), count);
     }

@@ -219,6 +219,25 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 // max(a, b, c) in one instruction
+// Two fp32 lanes per instruction (sm_100+ packed FP32): each lane rounds like
+// the scalar fmaf / add.  Half the FP32-pipe instructions of the scalar forms:
+// FP32-pipe issue on the sub-partition of the MMA-issuing warp delays its
+// tcgen05.mma issue, packed instructions much less so.
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b,
+                                          float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rd;\n\t"
+      "mov.b64 rd, {%0, %1};\n\tmov.b64 ra, {%2, %3};\n\t"
+      "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
