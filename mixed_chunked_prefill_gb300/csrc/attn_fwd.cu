@@ -122,6 +122,13 @@ __device__ __forceinline__ bool wait_on(const Ctx& c, uint32_t bar, uint32_t par
   return wait_slow(c.abort, c.err, bar, parity);
 }
 
+// wait_on for a warp that goes on to .sync.aligned tcgen05 instructions: every
+// lane gets the same answer, so a failed wait never leaves part of the warp
+// behind (each lane's own wait is bounded, so all of them reach the vote).
+__device__ __forceinline__ bool wait_on_warp(const Ctx& c, uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, wait_on(c, bar, parity));
+}
+
 // Bounded wait that ignores the abort flag: used to let this CTA's own async
 // copies / MMAs finish before it exits.
 __device__ __noinline__ void drain_wait(volatile int* abort, int32_t* err, uint32_t bar,
@@ -360,7 +367,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     jmax = jmax < kv1 - 1 ? jmax : kv1 - 1;
     const float sl2 = p.scale_log2;
     float m_ref = neg_inf(), l = 0.f;
-    bool ok = wait_on(c, c.b(BQ), 0);
+    bool ok = wait_on_warp(c, c.b(BQ), 0);
     {
       // Q is read for every KV tile: move this thread's row from the swizzled
       // shared-memory tile into TMEM (K-major, two bf16 per column) once, so
@@ -385,12 +392,13 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     }
     for (int t = 0; ok && t < ntiles; ++t) {
       const int s = t & 1;
-      if (!(ok = wait_on(c, c.b(BS0 + s), (t >> 1) & 1))) break;
+      if (!(ok = wait_on_warp(c, c.b(BS0 + s), (t >> 1) & 1))) break;
       ptx::tc_fence_after();
       uint32_t r[kKvTile];
 #pragma unroll
       for (int j = 0; j < kKvTile / 32; ++j) ptx::tmem_ld32(tS + s * kKvTile + j * 32, r + j * 32);
-      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < kKvTile / 32; ++j) ptx::tmem_wait_ld_dep(r + j * 32);
       const int key0 = kv0 + t * kKvTile;
       // max of the raw scores (sm_scale > 0 keeps the order), eight independent chains
       float mxp[8];
@@ -441,11 +449,11 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       ptx::tmem_st32(tS + s * kKvTile, r);
       ptx::tmem_st32(tS + s * kKvTile + 32, r + 32);
       if (t > 0 && __any_sync(0xffffffffu, rescale)) {
-        // P V of the previous tile must be done before O is rescaled: it frees
-        // stage (t-1) % 3.  That barrier is at most one phase off: its next use
-        // needs P(t+2), and S(t) ready implies every earlier MMA is complete.
+        // P V of the previous tile (issued by the other MMA warp) must be done
+        // before O is rescaled; its barrier (V stage (t-1) % 3) completes next
+        // only with P V(t+2), which needs P(t+2), so it is at most one phase off.
         const int ps = (t - 1) % C::kKStages;
-        if (!(ok = wait_on(c, c.b(BE0 + ps), ((t - 1) / C::kKStages) & 1))) break;
+        if (!(ok = wait_on_warp(c, c.b(BE0 + ps), ((t - 1) / C::kKStages) & 1))) break;
         ptx::tc_fence_after();
 #pragma unroll 1
         for (int j = 0; j < D / 32; ++j) {
@@ -463,8 +471,8 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       ptx::tc_fence_before();
       ptx::mbar_arrive(c.b(BP0 + (t & 1)));
     }
-    // every MMA of the item (the MMA warp commits this once, after the last P V)
-    if (ok && ntiles > 0) ok = wait_on(c, c.b(BDRAIN), 0);
+    // every MMA of the item (each issuing warp commits once after its last MMA)
+    if (ok && ntiles > 0) ok = wait_on_warp(c, c.b(BDRAIN), 0);
     ptx::tc_fence_after();
     const bool store = ok && valid && !*c.abort;
     const bool direct = it.part_row < 0;
