@@ -301,6 +301,89 @@ mcp_status mcp_mixed_attn_fwd_noalloc(const mcp_attn_desc* desc, const int32_t* 
                                       const int32_t* seqlens_k, void* out, float* lse,
                                       int32_t** error_word, void* stream);
 
+/* ------------------------------------------------------------------------- */
+/* One step from host memory, two steps in flight                            */
+/* ------------------------------------------------------------------------- */
+/*
+ * The whole step of [W] "输入组装" from host arrays: the step's metadata and
+ * new tokens are copied to the device, the new K/V are appended to the paged
+ * caches (a1), the fused forward runs (a2..a9), and out (and lse) are copied
+ * back to host memory.  Up to two steps are in flight: while step n's kernels
+ * run on the caller's stream, step n+1 is planned on the host and its inputs
+ * are copied in on a second stream, and step n's outputs are copied out on a
+ * third.  Each in-flight step has its own staging slot (device inputs,
+ * outputs, metadata and workspace; page-locked metadata, slot mapping and
+ * work lists), so no step overwrites buffers another still reads.  The
+ * append of step n+1 runs after the forward of step n on the caller's stream.
+ *
+ * Memory is caller-owned: mcp_host_step_arena_bytes() sizes a device arena and
+ * a page-locked host arena for two slots.  The library keeps only a small host
+ * object (two streams, six events) between mcp_host_step_create() and
+ * mcp_host_step_destroy().  One object is used by one host thread at a time.
+ */
+typedef struct mcp_host_step_limits {
+  int32_t max_tokens;        /* T of any step                                    */
+  int32_t max_seqs;          /* S of any step                                    */
+  int32_t max_pages_per_seq; /* row length of every step's block_tables          */
+  int32_t reserved0;         /* must be 0                                        */
+  int64_t workspace_bytes;   /* device workspace per slot (work lists + split
+                                partials, see mcp_plan); 0 = 64 MiB              */
+  int64_t list_bytes;        /* page-locked work-list bytes per slot; 0 = 4 MiB  */
+  int32_t reserved[4];       /* must be 0                                        */
+} mcp_host_step_limits;
+
+typedef struct mcp_host_step mcp_host_step; /* opaque */
+
+/*
+ * Bytes of the device arena and of the page-locked host arena for `limits`.
+ * shape supplies num_q_heads, num_kv_heads, head_dim, page_size, num_pages and
+ * sm_scale (validated as in mcp_mixed_attn_plan; its num_seqs, total_q and
+ * max_pages_per_seq are ignored).  Host-only.
+ */
+mcp_status mcp_host_step_arena_bytes(const mcp_attn_desc* shape, const mcp_host_step_limits* limits,
+                                     size_t* device_bytes, size_t* host_bytes);
+
+/*
+ * device_arena: device memory of the current device, 256-byte aligned.
+ * host_arena: page-locked host memory (cudaHostAlloc or cudaHostRegister),
+ * 256-byte aligned; rejected with MCP_ERR_INVALID_ARG if it is not page-locked.
+ * stream: the stream the kernels run on.  *step receives the object.
+ */
+mcp_status mcp_host_step_create(const mcp_attn_desc* shape, const mcp_host_step_limits* limits,
+                                void* device_arena, size_t device_bytes, void* host_arena,
+                                size_t host_bytes, void* stream, mcp_host_step** step);
+
+/*
+ * Enqueue one step.  HOST pointers: cu_seqlens_q [S+1], seqlens_k [S] and
+ * block_tables [S, max_pages_per_seq] int32 are read before the call returns;
+ * q [T, H_q, D], k_new / v_new [T, H_kv, D] bf16 are read by the asynchronous
+ * copy-in (keep them unchanged until mcp_host_step_wait(ticket) returns;
+ * page-locked memory lets the copies overlap the kernels); out [T, H_q, D]
+ * bf16 and lse [T, H_q] float32 (or NULL) are written by the copy-out (valid
+ * after mcp_host_step_wait(ticket)).  k_cache, v_cache: device caches as in
+ * mcp_paged_kv_append.  *ticket receives the step's number (0, 1, ...).
+ * Metadata errors (including a block-table page outside the pool) are
+ * returned before anything is enqueued.  Blocks only while the step two
+ * before this one is still running (its slot is reused); if that step failed
+ * on the device and was not waited for, its error is returned here and
+ * nothing is enqueued.
+ */
+mcp_status mcp_host_step_run(mcp_host_step* step, int32_t num_seqs, const int32_t* cu_seqlens_q,
+                             const int32_t* seqlens_k, const int32_t* block_tables,
+                             const void* q, const void* k_new, const void* v_new, void* k_cache,
+                             void* v_cache, void* out, float* lse, int64_t* ticket);
+
+/*
+ * Block until step `ticket` has finished (its outputs are in host memory) and
+ * return its device-side check: MCP_ERR_TIMEOUT or MCP_ERR_DEVICE_CHECK as in
+ * mcp_check_device_errors().  A step whose slot was already reused has been
+ * checked by then: MCP_OK.
+ */
+mcp_status mcp_host_step_wait(mcp_host_step* step, int64_t ticket);
+
+/* Wait for every step in flight, then free the object (NULL is ignored). */
+mcp_status mcp_host_step_destroy(mcp_host_step* step);
+
 /* Device-check bits written to an error word. */
 #define MCP_DEVERR_TIMEOUT 0x1      /* a bounded mbarrier wait gave up           */
 #define MCP_DEVERR_PAGE_RANGE 0x2   /* a block-table page id outside the pool    */

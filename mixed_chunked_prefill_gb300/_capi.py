@@ -68,6 +68,18 @@ class Plan(ctypes.Structure):
     ]
 
 
+class HostStepLimits(ctypes.Structure):
+    _fields_ = [
+        ("max_tokens", c_int32),
+        ("max_seqs", c_int32),
+        ("max_pages_per_seq", c_int32),
+        ("reserved0", c_int32),
+        ("workspace_bytes", c_int64),
+        ("list_bytes", c_int64),
+        ("reserved", c_int32 * 4),
+    ]
+
+
 # name -> (restype, argtypes); every symbol include/mcp.h declares
 SIGNATURES = {
     "mcp_status_string": (c_char_p, [c_int32]),
@@ -93,6 +105,16 @@ SIGNATURES = {
     "mcp_workspace_error_word": (c_void_p, [POINTER(Plan), c_void_p]),
     "mcp_merge_states": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
                                    c_void_p, c_void_p, c_void_p]),
+    "mcp_host_step_arena_bytes": (c_int32, [POINTER(AttnDesc), POINTER(HostStepLimits),
+                                            POINTER(c_size_t), POINTER(c_size_t)]),
+    "mcp_host_step_create": (c_int32, [POINTER(AttnDesc), POINTER(HostStepLimits), c_void_p,
+                                       c_size_t, c_void_p, c_size_t, c_void_p,
+                                       POINTER(c_void_p)]),
+    "mcp_host_step_run": (c_int32, [c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                    POINTER(c_int64)]),
+    "mcp_host_step_wait": (c_int32, [c_void_p, c_int64]),
+    "mcp_host_step_destroy": (c_int32, [c_void_p]),
 }
 
 _lib = None

@@ -597,3 +597,316 @@ mcp_status mcp_merge_states(const float* o_parts, const float* lse_parts, int32_
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// One step from host memory, two steps in flight ([W] "输入组装": write the new
+// K/V through the slot mapping, then attend).  Slot n % 2 stages step n.
+// Streams: copy-in (h2d), the caller's stream (kernels), copy-out (d2h);
+// events: staged (copy-in done), computed (kernels done), done (copy-out
+// done).  A slot is reused only after the host has seen its `done` event, so
+// none of its device or page-locked buffers is overwritten while in use.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+struct StepLayout {
+  // per-slot byte offsets; device slot
+  int64_t d_q, d_k, d_v, d_out, d_lse, d_meta, d_slots, d_ws, d_slot_bytes;
+  // page-locked host slot
+  int64_t h_meta, h_slots, h_lists, h_err, h_slot_bytes;
+  int64_t n_meta;  // int32 metadata words: cu (S+1) | seqlens_k (S) | block tables (S * mp)
+  int64_t ws_bytes, list_bytes;
+};
+
+mcp_status step_limits(const mcp_attn_desc* shape, const mcp_host_step_limits* lim,
+                       mcp_host_step_limits& out) {
+  if (!lim) return fail(MCP_ERR_INVALID_ARG, "limits is NULL");
+  if (!shape) return fail(MCP_ERR_INVALID_ARG, "shape is NULL");
+  mcp_attn_desc d = *shape;
+  d.num_seqs = 0;
+  d.total_q = 0;
+  d.max_pages_per_seq = 1;
+  mcp_status st = validate_desc(&d);
+  if (st != MCP_OK) return st;
+  if (lim->reserved0 != 0) return fail(MCP_ERR_INVALID_ARG, "limits->reserved0 must be 0");
+  for (int i = 0; i < 4; ++i)
+    if (lim->reserved[i] != 0) return fail(MCP_ERR_INVALID_ARG, "limits->reserved must be 0");
+  if (lim->max_tokens <= 0 || lim->max_seqs <= 0 || lim->max_pages_per_seq <= 0)
+    return fail(MCP_ERR_INVALID_ARG, "limits must be positive (tokens %d, seqs %d, pages %d)",
+                lim->max_tokens, lim->max_seqs, lim->max_pages_per_seq);
+  if (lim->workspace_bytes < 0 || lim->list_bytes < 0)
+    return fail(MCP_ERR_INVALID_ARG, "negative workspace or list bytes");
+  out = *lim;
+  if (out.workspace_bytes == 0) out.workspace_bytes = int64_t(64) << 20;
+  if (out.list_bytes == 0) out.list_bytes = int64_t(4) << 20;
+  return MCP_OK;
+}
+
+StepLayout step_layout(const mcp_attn_desc& s, const mcp_host_step_limits& lim) {
+  StepLayout L;
+  const int64_t T = lim.max_tokens, S = lim.max_seqs, mp = lim.max_pages_per_seq;
+  const int64_t qrow = static_cast<int64_t>(s.num_q_heads) * s.head_dim * 2;
+  const int64_t kvrow = static_cast<int64_t>(s.num_kv_heads) * s.head_dim * 2;
+  L.n_meta = (S + 1) + S + S * mp;
+  int64_t o = 0;
+  L.d_q = o;     o = align256(o + T * qrow);
+  L.d_k = o;     o = align256(o + T * kvrow);
+  L.d_v = o;     o = align256(o + T * kvrow);
+  L.d_out = o;   o = align256(o + T * qrow);
+  L.d_lse = o;   o = align256(o + T * s.num_q_heads * 4);
+  L.d_meta = o;  o = align256(o + L.n_meta * 4);
+  L.d_slots = o; o = align256(o + T * 8);
+  L.d_ws = o;    o = align256(o + lim.workspace_bytes);
+  L.d_slot_bytes = o;
+  o = 0;
+  L.h_meta = o;  o = align256(o + L.n_meta * 4);
+  L.h_slots = o; o = align256(o + T * 8);
+  L.h_lists = o; o = align256(o + lim.list_bytes);
+  L.h_err = o;   o = align256(o + 4);
+  L.h_slot_bytes = o;
+  L.ws_bytes = lim.workspace_bytes;
+  L.list_bytes = lim.list_bytes;
+  return L;
+}
+
+mcp_status error_bits_status(int32_t v) {
+  if (v & MCP_DEVERR_TIMEOUT)
+    return fail(MCP_ERR_TIMEOUT, "a device-side wait gave up (error bits 0x%x)", v);
+  if (v != 0) return fail(MCP_ERR_DEVICE_CHECK, "device range check failed (error bits 0x%x)", v);
+  return okay();
+}
+
+}  // namespace
+
+struct mcp_host_step {
+  struct Slot {
+    char* dev;
+    unsigned char* host;
+    cudaEvent_t staged = nullptr, computed = nullptr, done = nullptr;
+    int64_t ticket = -1;  // step staged in this slot and not yet checked, else -1
+  };
+  mcp_attn_desc shape;
+  mcp_host_step_limits lim;
+  StepLayout L;
+  cudaStream_t compute = nullptr, h2d = nullptr, d2h = nullptr;
+  Slot slot[2];
+  int64_t next = 0;
+
+  // Wait for the slot's step and turn its device error word into a status.
+  mcp_status settle(Slot& sl) {
+    if (sl.ticket < 0) return okay();
+    const cudaError_t e = cudaEventSynchronize(sl.done);
+    if (e != cudaSuccess) return fail(MCP_ERR_CUDA, "step %lld: %s", static_cast<long long>(sl.ticket),
+                                      cudaGetErrorString(e));
+    int32_t* err = reinterpret_cast<int32_t*>(sl.host + L.h_err);
+    const int32_t v = *err;
+    *err = 0;
+    sl.ticket = -1;
+    return error_bits_status(v);
+  }
+};
+
+extern "C" {
+
+mcp_status mcp_host_step_arena_bytes(const mcp_attn_desc* shape, const mcp_host_step_limits* limits,
+                                     size_t* device_bytes, size_t* host_bytes) {
+  mcp_host_step_limits lim;
+  mcp_status st = step_limits(shape, limits, lim);
+  if (st != MCP_OK) return st;
+  if (!device_bytes || !host_bytes) return fail(MCP_ERR_INVALID_ARG, "NULL size pointer");
+  const StepLayout L = step_layout(*shape, lim);
+  *device_bytes = static_cast<size_t>(2 * L.d_slot_bytes);
+  *host_bytes = static_cast<size_t>(2 * L.h_slot_bytes);
+  return okay();
+}
+
+mcp_status mcp_host_step_create(const mcp_attn_desc* shape, const mcp_host_step_limits* limits,
+                                void* device_arena, size_t device_bytes, void* host_arena,
+                                size_t host_bytes, void* stream, mcp_host_step** step) {
+  mcp_host_step_limits lim;
+  mcp_status st = step_limits(shape, limits, lim);
+  if (st != MCP_OK) return st;
+  if (!step) return fail(MCP_ERR_INVALID_ARG, "step is NULL");
+  *step = nullptr;
+  const StepLayout L = step_layout(*shape, lim);
+  if (!device_arena || !host_arena) return fail(MCP_ERR_INVALID_ARG, "NULL arena");
+  if (!aligned(device_arena, 256) || !aligned(host_arena, 256))
+    return fail(MCP_ERR_INVALID_ARG, "arenas must be 256-byte aligned");
+  if (static_cast<int64_t>(device_bytes) < 2 * L.d_slot_bytes ||
+      static_cast<int64_t>(host_bytes) < 2 * L.h_slot_bytes)
+    return fail(MCP_ERR_WORKSPACE_TOO_SMALL, "arenas %zu / %zu bytes < %lld / %lld needed",
+                device_bytes, host_bytes, static_cast<long long>(2 * L.d_slot_bytes),
+                static_cast<long long>(2 * L.h_slot_bytes));
+  cudaPointerAttributes pa;
+  cudaError_t e = cudaPointerGetAttributes(&pa, host_arena);
+  if (e != cudaSuccess) return fail(MCP_ERR_CUDA, "host arena query: %s", cudaGetErrorString(e));
+  if (pa.type != cudaMemoryTypeHost)
+    return fail(MCP_ERR_INVALID_ARG, "host arena is not page-locked host memory");
+  e = cudaPointerGetAttributes(&pa, device_arena);
+  if (e != cudaSuccess) return fail(MCP_ERR_CUDA, "device arena query: %s", cudaGetErrorString(e));
+  if (pa.type != cudaMemoryTypeDevice)
+    return fail(MCP_ERR_INVALID_ARG, "device arena is not device memory");
+  mcp_host_step* h = new (std::nothrow) mcp_host_step();
+  if (!h) return fail(MCP_ERR_INVALID_ARG, "host allocation failed");
+  h->shape = *shape;
+  h->lim = lim;
+  h->L = L;
+  h->compute = static_cast<cudaStream_t>(stream);
+  e = cudaStreamCreateWithFlags(&h->h2d, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->d2h, cudaStreamNonBlocking);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+    mcp_host_step::Slot& sl = h->slot[i];
+    sl.dev = static_cast<char*>(device_arena) + i * L.d_slot_bytes;
+    sl.host = static_cast<unsigned char*>(host_arena) + i * L.h_slot_bytes;
+    *reinterpret_cast<int32_t*>(sl.host + L.h_err) = 0;
+    e = cudaEventCreateWithFlags(&sl.staged, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sl.computed, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) {
+    mcp_host_step_destroy(h);
+    return fail(MCP_ERR_CUDA, "host step streams/events: %s", cudaGetErrorString(e));
+  }
+  *step = h;
+  return okay();
+}
+
+mcp_status mcp_host_step_run(mcp_host_step* step, int32_t num_seqs, const int32_t* cu_seqlens_q,
+                             const int32_t* seqlens_k, const int32_t* block_tables,
+                             const void* q, const void* k_new, const void* v_new, void* k_cache,
+                             void* v_cache, void* out, float* lse, int64_t* ticket) {
+  try {
+    if (!step) return fail(MCP_ERR_INVALID_ARG, "step is NULL");
+    if (!ticket) return fail(MCP_ERR_INVALID_ARG, "ticket is NULL");
+    const mcp_host_step_limits& lim = step->lim;
+    const StepLayout& L = step->L;
+    if (num_seqs < 0 || num_seqs > lim.max_seqs)
+      return fail(MCP_ERR_INVALID_ARG, "num_seqs %d outside [0, %d]", num_seqs, lim.max_seqs);
+    if (!cu_seqlens_q) return fail(MCP_ERR_INVALID_ARG, "cu_seqlens_q is NULL");
+    if (num_seqs > 0 && (!seqlens_k || !block_tables))
+      return fail(MCP_ERR_INVALID_ARG, "seqlens_k / block_tables is NULL");
+    const int32_t T = cu_seqlens_q[num_seqs];
+    if (T < 0 || T > lim.max_tokens)
+      return fail(MCP_ERR_INVALID_ARG, "step has %d tokens, limit %d", T, lim.max_tokens);
+    if (T > 0 && (!q || !k_new || !v_new || !out))
+      return fail(MCP_ERR_INVALID_ARG, "NULL token buffer");
+    if (!k_cache || !v_cache) return fail(MCP_ERR_INVALID_ARG, "NULL cache");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16))
+      return fail(MCP_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+
+    mcp_host_step::Slot& sl = step->slot[step->next & 1];
+    // the slot's previous step must be finished before its buffers are reused
+    mcp_status st = step->settle(sl);
+    if (st != MCP_OK) return st;
+
+    mcp_attn_desc desc = step->shape;
+    desc.num_seqs = num_seqs;
+    desc.total_q = T;
+    desc.max_pages_per_seq = lim.max_pages_per_seq;
+    mcp_plan plan;
+    Built b;
+    st = plan_common(&desc, cu_seqlens_q, seqlens_k, nullptr, &plan, b);
+    if (st != MCP_OK) return st;
+    if (plan.workspace_bytes > L.ws_bytes)
+      return fail(MCP_ERR_WORKSPACE_TOO_SMALL, "step needs %lld workspace bytes > limit %lld",
+                  static_cast<long long>(plan.workspace_bytes), static_cast<long long>(L.ws_bytes));
+    if (plan.off_part_o > L.list_bytes)
+      return fail(MCP_ERR_WORKSPACE_TOO_SMALL, "work lists need %lld bytes > limit %lld",
+                  static_cast<long long>(plan.off_part_o), static_cast<long long>(L.list_bytes));
+    // host staging: metadata, slot mapping (validates every page id), work lists
+    const int64_t S = num_seqs, mp = lim.max_pages_per_seq;
+    int32_t* hm = reinterpret_cast<int32_t*>(sl.host + L.h_meta);
+    int64_t* hs = reinterpret_cast<int64_t*>(sl.host + L.h_slots);
+    st = mcp_build_slot_mapping(block_tables, num_seqs, lim.max_pages_per_seq, desc.page_size,
+                                desc.num_pages, cu_seqlens_q, seqlens_k, hs);
+    if (st != MCP_OK) return st;
+    std::memcpy(hm, cu_seqlens_q, (S + 1) * sizeof(int32_t));
+    if (S > 0) {
+      std::memcpy(hm + S + 1, seqlens_k, S * sizeof(int32_t));
+      std::memcpy(hm + 2 * S + 1, block_tables, S * mp * sizeof(int32_t));
+    }
+    write_lists(plan, b, sl.host + L.h_lists);
+
+    char* dev = sl.dev;
+    int32_t* d_meta = reinterpret_cast<int32_t*>(dev + L.d_meta);
+    char* ws = dev + L.d_ws;
+    const int64_t n_meta = (S + 1) + S + S * mp;
+    const int64_t qbytes = static_cast<int64_t>(T) * desc.num_q_heads * desc.head_dim * 2;
+    const int64_t kvbytes = static_cast<int64_t>(T) * desc.num_kv_heads * desc.head_dim * 2;
+    const size_t lse_bytes = static_cast<size_t>(T) * desc.num_q_heads * 4;
+    cudaError_t e = cudaMemcpyAsync(d_meta, hm, n_meta * 4, cudaMemcpyHostToDevice, step->h2d);
+    if (e == cudaSuccess && T > 0)
+      e = cudaMemcpyAsync(dev + L.d_slots, hs, static_cast<size_t>(T) * 8, cudaMemcpyHostToDevice,
+                          step->h2d);
+    if (e == cudaSuccess && plan.off_part_o > 0)
+      e = cudaMemcpyAsync(ws, sl.host + L.h_lists, plan.off_part_o, cudaMemcpyHostToDevice, step->h2d);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws + plan.off_error, 0, 256, step->h2d);
+    if (e == cudaSuccess && T > 0) e = cudaMemcpyAsync(dev + L.d_q, q, qbytes, cudaMemcpyHostToDevice, step->h2d);
+    if (e == cudaSuccess && T > 0) e = cudaMemcpyAsync(dev + L.d_k, k_new, kvbytes, cudaMemcpyHostToDevice, step->h2d);
+    if (e == cudaSuccess && T > 0) e = cudaMemcpyAsync(dev + L.d_v, v_new, kvbytes, cudaMemcpyHostToDevice, step->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(sl.staged, step->h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(step->compute, sl.staged, 0);
+    if (e != cudaSuccess) return fail(MCP_ERR_CUDA, "step copy-in: %s", cudaGetErrorString(e));
+
+    int32_t* err_word = reinterpret_cast<int32_t*>(ws + plan.off_error);
+    if (T > 0) {
+      const int rc = mcp::launch_append(dev + L.d_k, dev + L.d_v,
+                                        reinterpret_cast<const int64_t*>(dev + L.d_slots), T,
+                                        desc.num_kv_heads * desc.head_dim * 2,
+                                        static_cast<int64_t>(desc.num_pages) * desc.page_size,
+                                        k_cache, v_cache, err_word, step->compute);
+      if (rc != 0) return cuda_fail(rc, "step append launch");
+    }
+    st = mcp_mixed_attn_fwd(&plan, dev + L.d_q, k_cache, v_cache, d_meta + 2 * S + 1, d_meta,
+                            d_meta + S + 1, dev + L.d_out,
+                            lse ? reinterpret_cast<float*>(dev + L.d_lse) : nullptr, ws,
+                            static_cast<size_t>(L.ws_bytes), step->compute);
+    if (st != MCP_OK) return st;
+    e = cudaEventRecord(sl.computed, step->compute);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(step->d2h, sl.computed, 0);
+    if (e == cudaSuccess && T > 0)
+      e = cudaMemcpyAsync(out, dev + L.d_out, qbytes, cudaMemcpyDeviceToHost, step->d2h);
+    if (e == cudaSuccess && T > 0 && lse)
+      e = cudaMemcpyAsync(lse, dev + L.d_lse, lse_bytes, cudaMemcpyDeviceToHost, step->d2h);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(sl.host + L.h_err, err_word, 4, cudaMemcpyDeviceToHost, step->d2h);
+    if (e == cudaSuccess) e = cudaEventRecord(sl.done, step->d2h);
+    if (e != cudaSuccess) return fail(MCP_ERR_CUDA, "step copy-out: %s", cudaGetErrorString(e));
+    sl.ticket = step->next;
+    *ticket = step->next++;
+    return okay();
+  } catch (const std::bad_alloc&) {
+    return fail(MCP_ERR_INVALID_ARG, "host allocation failed while planning");
+  } catch (...) {
+    return fail(MCP_ERR_INVALID_ARG, "unexpected host error in a step");
+  }
+}
+
+mcp_status mcp_host_step_wait(mcp_host_step* step, int64_t ticket) {
+  if (!step) return fail(MCP_ERR_INVALID_ARG, "step is NULL");
+  if (ticket < 0 || ticket >= step->next)
+    return fail(MCP_ERR_INVALID_ARG, "ticket %lld was never issued", static_cast<long long>(ticket));
+  for (mcp_host_step::Slot& sl : step->slot)
+    if (sl.ticket == ticket) return step->settle(sl);
+  return okay();  // its slot was reused, which checked it
+}
+
+mcp_status mcp_host_step_destroy(mcp_host_step* step) {
+  if (!step) return okay();
+  mcp_status st = MCP_OK;
+  for (mcp_host_step::Slot& sl : step->slot) {
+    const mcp_status s2 = step->settle(sl);
+    if (st == MCP_OK) st = s2;
+  }
+  for (mcp_host_step::Slot& sl : step->slot) {
+    if (sl.staged) cudaEventDestroy(sl.staged);
+    if (sl.computed) cudaEventDestroy(sl.computed);
+    if (sl.done) cudaEventDestroy(sl.done);
+  }
+  if (step->h2d) cudaStreamDestroy(step->h2d);
+  if (step->d2h) cudaStreamDestroy(step->d2h);
+  delete step;
+  return st == MCP_OK ? okay() : st;
+}
+
+}  // extern "C"

@@ -5,8 +5,10 @@ paged attention).
 
 ``MixedStep`` keeps one step's metadata, plan and workspace on the device and
 runs append + attention on device tensors.  ``HostStep`` is the end-to-end
-path from host buffers: it copies the step's inputs and metadata to the
-device, plans, runs, and copies the output back, all on one stream.
+path from host buffers over the library's pipelined host step: each call
+copies the step's inputs and metadata to the device, plans on the host,
+appends, attends and copies the output back, with up to two steps in flight
+(the copies of one step overlap the kernels of the other).
 """
 
 from __future__ import annotations
@@ -94,85 +96,121 @@ def write_history(block_tables, hist_lens, k_hist, v_hist, k_cache, v_cache, pag
 
 
 class HostStep:
-    """End-to-end step from host memory.
+    """End-to-end steps from host memory (``mcp_host_step_*``).
 
-    Per call: host->device copies of q, k_new, v_new and the metadata (block
-    tables, cu_seqlens_q, seqlens_k, slot mapping) from pinned buffers; host
-    planning and plan upload; append; attention; device->host copy of the
-    output into a pinned buffer.  The KV cache is device-resident state.
+    ``run`` enqueues one step and returns its ticket without waiting: the
+    copy-in of q, k_new, v_new (page-locked host tensors, left unchanged until
+    the step is waited for), host planning, append, attention and the
+    copy-out into ``out_h`` (and ``lse_h``).  ``wait(ticket)`` blocks until
+    that step's outputs are in host memory and raises on a device-side error.
+    Calling the object runs one step and waits for it.  The device and
+    page-locked arenas are torch tensors owned by this object; the KV cache
+    is the caller's device state.
     """
 
     def __init__(self, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, sm_scale,
-                 max_tokens, max_seqs, max_pages_per_seq, device="cuda", options=None,
-                 stream=None, workspace_bytes=1 << 26):
+                 max_tokens, max_seqs, max_pages_per_seq, device="cuda", stream=None,
+                 workspace_bytes=0, list_bytes=0):
+        import ctypes
+
         import torch
 
+        from . import _capi, load
+
+        self._lib = load()
         self.hq, self.hkv, self.D, self.P = num_q_heads, num_kv_heads, head_dim, page_size
-        self.num_pages, self.scale = num_pages, sm_scale
-        self.options = options
-        self.stream = stream if stream is not None else torch.cuda.current_stream()
-        dev = device
-        self.q_d = torch.empty((max_tokens, num_q_heads, head_dim), dtype=torch.bfloat16, device=dev)
-        self.k_d = torch.empty((max_tokens, num_kv_heads, head_dim), dtype=torch.bfloat16, device=dev)
-        self.v_d = torch.empty_like(self.k_d)
-        self.out_d = torch.empty_like(self.q_d)
-        self.cu_d = torch.empty(max_seqs + 1, dtype=torch.int32, device=dev)
-        self.sk_d = torch.empty(max_seqs, dtype=torch.int32, device=dev)
-        self.bt_d = torch.empty((max_seqs, max_pages_per_seq), dtype=torch.int32, device=dev)
-        self.slots_d = torch.empty(max_tokens, dtype=torch.int64, device=dev)
-        self.meta_h = torch.empty(max_seqs * (max_pages_per_seq + 2) + 1, dtype=torch.int32,
-                                  pin_memory=True)
-        self.slots_h = torch.empty(max_tokens, dtype=torch.int64, pin_memory=True)
-        self.workspace = torch.empty(workspace_bytes, dtype=torch.uint8, device=dev)
+        self.mp = int(max_pages_per_seq)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(device)
+        shape = make_desc(0, 0, num_q_heads, num_kv_heads, head_dim, page_size, 1, num_pages,
+                          sm_scale)
+        lim = _capi.HostStepLimits(int(max_tokens), int(max_seqs), self.mp, 0,
+                                   int(workspace_bytes), int(list_bytes), (ctypes.c_int32 * 4)())
+        dbytes, hbytes = ctypes.c_size_t(), ctypes.c_size_t()
+        _capi.check(self._lib.mcp_host_step_arena_bytes(ctypes.byref(shape), ctypes.byref(lim),
+                                                        ctypes.byref(dbytes), ctypes.byref(hbytes)),
+                    "host_step_arena_bytes")
+        # arenas: torch's device and page-locked allocations are 256-byte aligned
+        self.device_arena = torch.empty(dbytes.value, dtype=torch.uint8, device=device)
+        self.host_arena = torch.empty(hbytes.value, dtype=torch.uint8, pin_memory=True)
+        handle = ctypes.c_void_p()
+        _capi.check(self._lib.mcp_host_step_create(
+            ctypes.byref(shape), ctypes.byref(lim), ctypes.c_void_p(self.device_arena.data_ptr()),
+            dbytes.value, ctypes.c_void_p(self.host_arena.data_ptr()), hbytes.value,
+            ctypes.c_void_p(self.stream.cuda_stream), ctypes.byref(handle)), "host_step_create")
+        self._h = handle
+        self._keep = {}  # host arrays a ticket's copies still read / write
         self.h2d_bytes = 0
         self.d2h_bytes = 0
 
-    def __call__(self, q_h, k_new_h, v_new_h, cu_seqlens_q, seqlens_k, block_tables, k_cache,
-                 v_cache, out_h):
-        """q_h / k_new_h / v_new_h / out_h: pinned host bf16 tensors; metadata:
-        host int arrays.  Returns out_h after the device->host copy finished."""
+    def run(self, q_h, k_new_h, v_new_h, cu_seqlens_q, seqlens_k, block_tables, k_cache,
+            v_cache, out_h, lse_h=None) -> int:
+        import ctypes
+
         import torch
+
+        from . import _capi
 
         cu = _i32(cu_seqlens_q)
         sk = _i32(seqlens_k)
         bt = _i32(block_tables)
-        S, T = len(sk), int(cu[-1])
-        mp = bt.shape[1]
-        slots = build_slot_mapping(bt, cu, sk, self.P, self.num_pages)
-        desc = make_desc(S, T, self.hq, self.hkv, self.D, self.P, mp, self.num_pages, self.scale)
-        plan = mixed_attn_plan(desc, cu, sk, self.options)
-        if plan.workspace_bytes > self.workspace.numel():
-            self.workspace = torch.empty(int(plan.workspace_bytes), dtype=torch.uint8,
-                                         device=self.workspace.device)
-        # pack metadata into one pinned buffer -> one copy
-        n_meta = (S + 1) + S + S * mp
-        meta = self.meta_h[:n_meta].numpy()
-        meta[:S + 1] = cu
-        meta[S + 1:2 * S + 1] = sk
-        meta[2 * S + 1:] = bt.reshape(-1)
-        self.slots_h[:T].numpy()[:] = slots
-        s = self.stream
-        with torch.cuda.stream(s):
-            meta_d = torch.empty(n_meta, dtype=torch.int32, device=self.cu_d.device)
-            meta_d.copy_(self.meta_h[:n_meta], non_blocking=True)
-            cu_d = meta_d[:S + 1]
-            sk_d = meta_d[S + 1:2 * S + 1]
-            bt_d = meta_d[2 * S + 1:].view(S, mp)
-            slots_d = self.slots_d[:T]
-            slots_d.copy_(self.slots_h[:T], non_blocking=True)
-            q_d = self.q_d[:T]
-            k_d = self.k_d[:T]
-            v_d = self.v_d[:T]
-            q_d.copy_(q_h, non_blocking=True)
-            k_d.copy_(k_new_h, non_blocking=True)
-            v_d.copy_(v_new_h, non_blocking=True)
-            plan = mixed_attn_plan(desc, cu, sk, self.options, self.workspace, s)
-            paged_kv_append(k_d, v_d, slots_d, k_cache, v_cache, stream=s)
-            out_d = self.out_d[:T]
-            mixed_attn_fwd(plan, q_d, k_cache, v_cache, bt_d, cu_d, sk_d, out_d, None,
-                           self.workspace, s)
-            out_h.copy_(out_d, non_blocking=True)
-        self.h2d_bytes = (n_meta * 4 + T * 8 + q_h.numel() * 2 + k_new_h.numel() * 2
-                          + v_new_h.numel() * 2)
-        self.d2h_bytes = out_h.numel() * 2
+        S = len(sk)
+        if bt.ndim != 2 or bt.shape[0] != S or bt.shape[1] > self.mp:
+            raise ValueError(f"block_tables must be [S, <= {self.mp}]")
+        if bt.shape[1] < self.mp:
+            full = np.full((S, self.mp), -1, dtype=np.int32)
+            full[:, :bt.shape[1]] = bt
+            bt = full
+        T = int(cu[-1]) if len(cu) else 0
+        for t, name, dt in ((q_h, "q", torch.bfloat16), (k_new_h, "k_new", torch.bfloat16),
+                            (v_new_h, "v_new", torch.bfloat16), (out_h, "out", torch.bfloat16)):
+            if t.is_cuda or t.dtype != dt or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous host {dt} tensor")
+        if lse_h is not None and (lse_h.is_cuda or lse_h.dtype != torch.float32):
+            raise ValueError("lse must be a host float32 tensor")
+        if q_h.numel() < T * self.hq * self.D or out_h.numel() < T * self.hq * self.D:
+            raise ValueError("q / out smaller than [T, H_q, D]")
+        if k_new_h.numel() < T * self.hkv * self.D or v_new_h.numel() < T * self.hkv * self.D:
+            raise ValueError("k_new / v_new smaller than [T, H_kv, D]")
+        ticket = ctypes.c_int64(-1)
+        st = self._lib.mcp_host_step_run(
+            self._h, S, cu.ctypes.data_as(ctypes.c_void_p), sk.ctypes.data_as(ctypes.c_void_p),
+            bt.ctypes.data_as(ctypes.c_void_p), ctypes.c_void_p(q_h.data_ptr()),
+            ctypes.c_void_p(k_new_h.data_ptr()), ctypes.c_void_p(v_new_h.data_ptr()),
+            ctypes.c_void_p(k_cache.data_ptr()), ctypes.c_void_p(v_cache.data_ptr()),
+            ctypes.c_void_p(out_h.data_ptr()),
+            ctypes.c_void_p(lse_h.data_ptr()) if lse_h is not None else None, ctypes.byref(ticket))
+        _capi.check(st, "host_step_run")
+        t = int(ticket.value)
+        self._keep[t] = (q_h, k_new_h, v_new_h, out_h, lse_h)
+        for old in [k for k in self._keep if k < t - 1]:
+            del self._keep[old]  # slot reused: that step has finished
+        self.h2d_bytes = (cu.nbytes + sk.nbytes + bt.nbytes + T * 8
+                          + 2 * T * (self.hq + 2 * self.hkv) * self.D)
+        self.d2h_bytes = 2 * T * self.hq * self.D + (4 * T * self.hq if lse_h is not None else 0)
+        return t
+
+    def wait(self, ticket: int):
+        from . import _capi
+
+        _capi.check(self._lib.mcp_host_step_wait(self._h, int(ticket)), "host_step_wait")
+        self._keep.pop(int(ticket), None)
+
+    def __call__(self, q_h, k_new_h, v_new_h, cu_seqlens_q, seqlens_k, block_tables, k_cache,
+                 v_cache, out_h, lse_h=None):
+        self.wait(self.run(q_h, k_new_h, v_new_h, cu_seqlens_q, seqlens_k, block_tables,
+                           k_cache, v_cache, out_h, lse_h))
         return out_h
+
+    def close(self):
+        from . import _capi
+
+        if getattr(self, "_h", None) is not None and self._h.value:
+            h, self._h = self._h, None
+            _capi.check(self._lib.mcp_host_step_destroy(h), "host_step_destroy")
+            self._keep.clear()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
