@@ -302,6 +302,57 @@ mcp_status mcp_mixed_attn_fwd_noalloc(const mcp_attn_desc* desc, const int32_t* 
                                       int32_t** error_word, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* Sampled rows: logits_indices, attention for listed rows, row gather       */
+/* ------------------------------------------------------------------------- */
+/*
+ * [W] "采样：只有该出字的请求才出字": the output layer computes logits only at
+ * the last position of every segment, logits_indices = query_start_loc[1:] - 1,
+ * and the sampler keeps them only for decode segments and for chunks that
+ * finish their prompt.  Host-only: h_out receives the index of the last token
+ * of every segment with at least one token this step, in segment order, and
+ * *count their number (at most num_seqs).  h_sample_mask [S] (or NULL = all):
+ * segments with mask 0 are left out.  A segment without tokens contributes no
+ * index (the printed formula would name the previous segment's last token).
+ */
+mcp_status mcp_build_logits_indices(int32_t num_seqs, const int32_t* h_cu_seqlens_q,
+                                    const uint8_t* h_sample_mask, int32_t* h_out,
+                                    int32_t* count);
+
+/*
+ * Plan attention for the listed query rows only (e.g. logits_indices in the
+ * last layer, where only the sampled positions feed the output head).
+ * h_rows [num_rows]: HOST token indices into the packed stream, strictly
+ * increasing, each in [0, total_q).  Each listed token attends exactly as in
+ * the full step (its segment's paged KV, right-aligned causal); rows of out /
+ * lse not listed are not written by mcp_mixed_attn_fwd with this plan.
+ * Consecutive listed tokens of one segment share a work item.  Everything
+ * else as mcp_mixed_attn_plan (workspace NULL = sizing only).
+ */
+mcp_status mcp_mixed_attn_plan_rows(const mcp_attn_desc* desc, const int32_t* h_cu_seqlens_q,
+                                    const int32_t* h_seqlens_k, const int32_t* h_rows,
+                                    int32_t num_rows, const mcp_plan_options* opts,
+                                    mcp_plan* plan, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/* mcp_mixed_attn_plan_rows that writes the work lists into a HOST buffer (as
+ * mcp_mixed_attn_plan_host; host_buffer NULL = sizing only). */
+mcp_status mcp_mixed_attn_plan_rows_host(const mcp_attn_desc* desc, const int32_t* h_cu_seqlens_q,
+                                         const int32_t* h_seqlens_k, const int32_t* h_rows,
+                                         int32_t num_rows, const mcp_plan_options* opts,
+                                         mcp_plan* plan, void* host_buffer, size_t host_bytes);
+
+/*
+ * dst[i][:] = src[rows[i]][:] for i < num_rows (device; rows of row_bytes
+ * bytes, bit-exact) -- e.g. the attention output [T, H_q, D] at
+ * logits_indices, packed for the output head.  row_bytes % 16 == 0; src, dst
+ * 16-byte aligned; rows: device int32.  An index outside [0, num_src_rows)
+ * writes a zero row and sets MCP_DEVERR_ROW_RANGE in error_word (if not NULL).
+ */
+mcp_status mcp_gather_rows(const void* src, int32_t num_src_rows, int32_t row_bytes,
+                           const int32_t* rows, int32_t num_rows, void* dst, int32_t* error_word,
+                           void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* One step from host memory, two steps in flight                            */
 /* ------------------------------------------------------------------------- */
 /*
@@ -388,6 +439,7 @@ mcp_status mcp_host_step_destroy(mcp_host_step* step);
 #define MCP_DEVERR_TIMEOUT 0x1      /* a bounded mbarrier wait gave up           */
 #define MCP_DEVERR_PAGE_RANGE 0x2   /* a block-table page id outside the pool    */
 #define MCP_DEVERR_SLOT_RANGE 0x4   /* an append slot outside the pool           */
+#define MCP_DEVERR_ROW_RANGE 0x8    /* a gathered row index outside the source   */
 
 #ifdef __cplusplus
 }

@@ -28,6 +28,7 @@ __all__ = [
     "AttnDesc", "Plan", "PlanOptions", "MCPError", "load", "abi_version", "paged_kv_append",
     "build_slot_mapping", "mixed_attn_plan", "mixed_attn_fwd", "check_device_errors",
     "workspace_error_word", "merge_states", "make_desc", "mixed_attn_fwd_noalloc",
+    "mixed_attn_plan_rows", "build_logits_indices", "gather_rows",
 ]
 
 
@@ -138,6 +139,69 @@ def mixed_attn_plan(desc: AttnDesc, cu_seqlens_q, seqlens_k, options: PlanOption
                                  _stream(stream) if workspace is not None else None)
     _capi.check(st, "mixed_attn_plan")
     return plan
+
+
+def mixed_attn_plan_rows(desc: AttnDesc, cu_seqlens_q, seqlens_k, rows,
+                         options: PlanOptions | None = None, workspace=None,
+                         stream=None) -> Plan:
+    """Plan attention for the listed query rows only (HOST token indices,
+    strictly increasing); with ``workspace`` also copy the work lists into it."""
+    import torch
+
+    lib = load()
+    cu, cu_p = _host_i32(cu_seqlens_q, "cu_seqlens_q")
+    sk, sk_p = _host_i32(seqlens_k, "seqlens_k")
+    rw, rw_p = _host_i32(rows, "rows")
+    plan = Plan()
+    ws = _dev(workspace, torch.uint8, "workspace") if workspace is not None else None
+    nbytes = int(workspace.numel()) if workspace is not None else 0
+    st = lib.mcp_mixed_attn_plan_rows(ctypes.byref(desc), cu_p, sk_p, rw_p, int(rw.size),
+                                      ctypes.byref(options) if options is not None else None,
+                                      ctypes.byref(plan), ws, nbytes,
+                                      _stream(stream) if workspace is not None else None)
+    _capi.check(st, "mixed_attn_plan_rows")
+    return plan
+
+
+def build_logits_indices(cu_seqlens_q, sample_mask=None) -> np.ndarray:
+    """The last token of every segment with a token this step (optionally only
+    segments with a non-zero ``sample_mask``): int32 numpy array."""
+    lib = load()
+    cu, cu_p = _host_i32(cu_seqlens_q, "cu_seqlens_q")
+    S = int(cu.size) - 1
+    out = np.empty(max(S, 1), dtype=np.int32)
+    count = ctypes.c_int32()
+    mask_p = None
+    if sample_mask is not None:
+        m = np.ascontiguousarray(np.asarray(sample_mask, dtype=np.uint8))
+        if m.size != S:
+            raise ValueError("sample_mask must have one entry per segment")
+        mask_p = m.ctypes.data_as(ctypes.c_void_p)
+    st = lib.mcp_build_logits_indices(S, cu_p, mask_p, out.ctypes.data_as(ctypes.c_void_p),
+                                      ctypes.byref(count))
+    _capi.check(st, "build_logits_indices")
+    return out[:count.value].copy()
+
+
+def gather_rows(src, rows, dst, error_word=None, stream=None) -> None:
+    """dst[i] = src[rows[i]] along the first dimension (device tensors; rows int32)."""
+    import torch
+
+    lib = load()
+    n = int(rows.numel())
+    if dst.shape[0] != n or tuple(dst.shape[1:]) != tuple(src.shape[1:]) or dst.dtype != src.dtype:
+        raise ValueError("dst must be [len(rows), *src.shape[1:]] of src's dtype")
+    if not (src.is_cuda and dst.is_cuda and src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("src / dst must be contiguous CUDA tensors")
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else dst[0].numel() * dst.element_size()
+    if error_word is None or isinstance(error_word, torch.Tensor):
+        ew = _dev(error_word, torch.int32, "error_word")
+    else:
+        ew = ctypes.c_void_p(int(error_word))
+    st = lib.mcp_gather_rows(ctypes.c_void_p(src.data_ptr()), int(src.shape[0]), int(row_bytes),
+                             _dev(rows, torch.int32, "rows"), n, ctypes.c_void_p(dst.data_ptr()),
+                             ew, _stream(stream))
+    _capi.check(st, "gather_rows")
 
 
 def mixed_attn_fwd(plan: Plan, q, k_cache, v_cache, block_tables, cu_seqlens_q, seqlens_k, out,

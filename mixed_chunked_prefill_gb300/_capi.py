@@ -105,6 +105,16 @@ SIGNATURES = {
     "mcp_workspace_error_word": (c_void_p, [POINTER(Plan), c_void_p]),
     "mcp_merge_states": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
                                    c_void_p, c_void_p, c_void_p]),
+    "mcp_build_logits_indices": (c_int32, [c_int32, c_void_p, c_void_p, c_void_p,
+                                           POINTER(c_int32)]),
+    "mcp_mixed_attn_plan_rows": (c_int32, [POINTER(AttnDesc), c_void_p, c_void_p, c_void_p,
+                                           c_int32, POINTER(PlanOptions), POINTER(Plan),
+                                           c_void_p, c_size_t, c_void_p]),
+    "mcp_mixed_attn_plan_rows_host": (c_int32, [POINTER(AttnDesc), c_void_p, c_void_p,
+                                                c_void_p, c_int32, POINTER(PlanOptions),
+                                                POINTER(Plan), c_void_p, c_size_t]),
+    "mcp_gather_rows": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p,
+                                  c_void_p, c_void_p]),
     "mcp_host_step_arena_bytes": (c_int32, [POINTER(AttnDesc), POINTER(HostStepLimits),
                                             POINTER(c_size_t), POINTER(c_size_t)]),
     "mcp_host_step_create": (c_int32, [POINTER(AttnDesc), POINTER(HostStepLimits), c_void_p,

@@ -1,4 +1,5 @@
-// Paged KV append: scatter each new token's K/V row into its physical slot.
+// Row copies of the step: the paged KV append (scatter each new token's K/V
+// row into its physical slot) and the row gather of the sampled positions.
 //
 // [W] "输入组装": the new tokens' K/V are written into the paged cache through
 // slot_mapping before attention runs; [L] 4.2 (append_paged_kv_cache):
@@ -38,7 +39,51 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(
   }
 }
 
+// dst[i] = src[rows[i]] ([W] "采样：只有该出字的请求才出字": the output rows at
+// logits_indices), 16-byte vectors, consecutive threads on consecutive vectors
+// of a row.  An index outside the source is reported and its row zeroed.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
+                                                          int32_t num_src_rows,
+                                                          const int32_t* __restrict__ rows,
+                                                          int64_t total_vec, int32_t vec_per_row,
+                                                          uint4* __restrict__ dst, int32_t* err) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vec;
+       i += stride) {
+    const int64_t r = i / vec_per_row;
+    const int64_t c = i - r * vec_per_row;
+    const int32_t from = rows[r];
+    if (from < 0 || from >= num_src_rows) {
+      if (err && c == 0) atomicOr(err, MCP_DEVERR_ROW_RANGE);
+      dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    dst[i] = src[static_cast<int64_t>(from) * vec_per_row + c];
+  }
+}
+
+int grid_for(int64_t total) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  return static_cast<int>(blocks > cap ? cap : blocks);
+}
+
 }  // namespace
+
+int launch_gather_rows(const void* src, int32_t num_src_rows, int32_t row_bytes,
+                       const int32_t* rows, int32_t num_rows, void* dst, int32_t* error_word,
+                       void* stream) {
+  if (num_rows <= 0) return 0;
+  const int32_t vec = row_bytes / 16;
+  const int64_t total = static_cast<int64_t>(num_rows) * vec;
+  gather_rows_kernel<<<grid_for(total), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(src), num_src_rows, rows, total, vec, static_cast<uint4*>(dst),
+      error_word);
+  return static_cast<int>(cudaGetLastError());
+}
 
 int launch_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
                   int32_t num_tokens, int32_t row_bytes, int64_t num_slots, void* k_cache,
@@ -46,13 +91,7 @@ int launch_append(const void* k_new, const void* v_new, const int64_t* slot_mapp
   if (num_tokens <= 0) return 0;
   const int32_t vec_per_tok = row_bytes / 16;
   const int64_t total = static_cast<int64_t>(num_tokens) * vec_per_tok;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  int64_t blocks = (total + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;
-  if (blocks > cap) blocks = cap;
-  paged_kv_append_kernel<<<static_cast<int>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+  paged_kv_append_kernel<<<grid_for(total), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, total,
       vec_per_tok, num_slots, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
       error_word);

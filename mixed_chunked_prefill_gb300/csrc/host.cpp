@@ -121,31 +121,74 @@ void even_split(int64_t len, int64_t cap, int64_t gran, int64_t* n, int64_t* siz
   *n = cdiv(len, sz);
 }
 
-void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num_sms,
-           const mcp_plan_options* o, Built& b) {
+// A unit of query rows the planner cuts into work items: tokens [qb, qb + qc)
+// of segment s, on the decode path (qc * G <= 16 rows) or the tensor-core path.
+struct Unit {
+  int s;
+  int64_t qb, qc;
+  bool decode;
+};
+
+// Units of a whole step: each decode segment whole, each chunk by 128-row
+// tiles.  With `rows` (strictly increasing token indices): only those tokens,
+// consecutive tokens of one segment grouped (at most 16 query rows on the
+// decode path; a lone token of G > 16 heads takes a tensor-core tile).
+std::vector<Unit> plan_units(const mcp_attn_desc& d, const int32_t* cu, const int32_t* rows,
+                             int32_t num_rows) {
   const int G = d.num_q_heads / d.num_kv_heads;
   const int TQ = mcp::kTileRows / G;
+  std::vector<Unit> u;
+  if (!rows) {
+    for (int s = 0; s < d.num_seqs; ++s) {
+      const int64_t lq = cu[s + 1] - cu[s];
+      if (lq == 0) continue;
+      if (lq * G <= mcp::kDecodeMaxRows) {
+        u.push_back({s, 0, lq, true});
+      } else {
+        for (int64_t qb = 0; qb < lq; qb += TQ) u.push_back({s, qb, std::min<int64_t>(TQ, lq - qb), false});
+      }
+    }
+    return u;
+  }
+  const int64_t dec_max = std::max(1, mcp::kDecodeMaxRows / G);  // tokens per decode unit
+  int s = 0;
+  for (int32_t i = 0; i < num_rows;) {
+    const int32_t t = rows[i];
+    while (cu[s + 1] <= t) ++s;
+    const bool dec = G <= mcp::kDecodeMaxRows;
+    const int64_t cap = dec ? dec_max : TQ;
+    int32_t j = i + 1;
+    while (j < num_rows && rows[j] == rows[j - 1] + 1 && rows[j] < cu[s + 1] && j - i < cap) ++j;
+    u.push_back({s, t - cu[s], j - i, dec});
+    i = j;
+  }
+  return u;
+}
+
+void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num_sms,
+           const mcp_plan_options* o, Built& b, const int32_t* rows = nullptr,
+           int32_t num_rows = 0) {
+  const int G = d.num_q_heads / d.num_kv_heads;
   const int H = d.num_kv_heads;
   const int HG = mcp::decode_head_group(H);
   const int dopt = o ? o->decode_split_tokens : 0;
   const int popt = o ? o->prefill_split_tokens : 0;
+  const std::vector<Unit> units = plan_units(d, cu, rows, num_rows);
+  // keys visible to the unit's last token (right-aligned causal)
+  auto vis_of = [&](const Unit& x) {
+    return static_cast<int64_t>(sk[x.s]) - (cu[x.s + 1] - cu[x.s]) + x.qb + x.qc;
+  };
 
   auto count = [&](int64_t ds, int64_t ps) {
     int64_t n = 0;
-    for (int s = 0; s < d.num_seqs; ++s) {
-      const int64_t lq = cu[s + 1] - cu[s], lk = sk[s];
-      if (lq == 0) continue;
-      if (lq * G <= mcp::kDecodeMaxRows) {
-        int64_t k, z;
-        even_split(lk, ds, mcp::kPageSize, &k, &z);
+    for (const Unit& x : units) {
+      int64_t k, z;
+      if (x.decode) {
+        even_split(vis_of(x), ds, mcp::kPageSize, &k, &z);
         n += k * (H / HG);
       } else {
-        for (int64_t qb = 0; qb < lq; qb += TQ) {
-          const int64_t vis = lk - lq + std::min<int64_t>(lq, qb + TQ);
-          int64_t k, z;
-          even_split(vis, ps, mcp::kKvTile, &k, &z);
-          n += k * H;
-        }
+        even_split(vis_of(x), ps, mcp::kKvTile, &k, &z);
+        n += k * H;
       }
     }
     return n;
@@ -158,10 +201,8 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
     ds = round_up(dopt, mcp::kPageSize);
   } else {
     int64_t dec_tokens = 0;
-    for (int s = 0; s < d.num_seqs; ++s) {
-      const int64_t lq = cu[s + 1] - cu[s];
-      if (lq > 0 && lq * G <= mcp::kDecodeMaxRows) dec_tokens += sk[s] * (H / HG);
-    }
+    for (const Unit& x : units)
+      if (x.decode) dec_tokens += vis_of(x) * (H / HG);
     ds = std::max<int64_t>(1024, round_up(cdiv(dec_tokens, 8LL * num_sms), mcp::kPageSize));
   }
   int64_t ps = popt > 0 ? round_up(popt, mcp::kKvTile) : 32768;
@@ -183,22 +224,23 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
     int64_t group;
   };
   std::vector<Entry> dec, pre;
-  for (int s = 0; s < d.num_seqs; ++s) {
-    const int64_t lq = cu[s + 1] - cu[s], lk = sk[s], hist = lk - lq;
-    if (lq == 0) continue;
-    if (lq * G <= mcp::kDecodeMaxRows) {
+  for (const Unit& x : units) {
+    const int s = x.s;
+    const int64_t vis = vis_of(x);
+    const int rows_n = static_cast<int>(x.qc * G);
+    if (x.decode) {
       int64_t n, sz;
-      even_split(lk, ds, mcp::kPageSize, &n, &sz);
-      const int rows = static_cast<int>(lq * G);
+      even_split(vis, ds, mcp::kPageSize, &n, &sz);
       for (int h0 = 0; h0 < H; h0 += HG) {
         int64_t base = -1;
         if (n > 1) {
           // head j of the group, split k: partial rows base + j*n*rows + k*rows
           base = b.part_rows;
-          b.part_rows += n * rows * HG;
+          b.part_rows += n * rows_n * HG;
           for (int j = 0; j < HG; ++j)
-            b.comb.push_back({s, h0 + j, 0, static_cast<int32_t>(lq), static_cast<int32_t>(n),
-                              static_cast<int32_t>(base + j * n * rows), rows, 0});
+            b.comb.push_back({s, h0 + j, static_cast<int32_t>(x.qb), static_cast<int32_t>(x.qc),
+                              static_cast<int32_t>(n), static_cast<int32_t>(base + j * n * rows_n),
+                              rows_n, 0});
         }
         for (int64_t k = 0; k < n; ++k) {
           mcp::WorkItem it;
@@ -206,47 +248,42 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
           it.kv_head = static_cast<int16_t>(h0);
           it.kind = mcp::kDecodeItem;
           it.num_heads = static_cast<int8_t>(HG);
-          it.q_begin = 0;
-          it.q_count = static_cast<int32_t>(lq);
+          it.q_begin = static_cast<int32_t>(x.qb);
+          it.q_count = static_cast<int32_t>(x.qc);
           it.kv_begin = static_cast<int32_t>(k * sz);
-          it.kv_end = static_cast<int32_t>(std::min(lk, (k + 1) * sz));
-          it.part_row = static_cast<int32_t>(n > 1 ? base + k * rows : -1);
-          it.part_head_stride = static_cast<int32_t>(n * rows);
+          it.kv_end = static_cast<int32_t>(std::min(vis, (k + 1) * sz));
+          it.part_row = static_cast<int32_t>(n > 1 ? base + k * rows_n : -1);
+          it.part_head_stride = static_cast<int32_t>(n * rows_n);
           dec.push_back({it, (it.kv_end - it.kv_begin) * 4.0 * d.head_dim * HG / 45.0, 0});
         }
       }
     } else {
-      for (int64_t qb = 0; qb < lq; qb += TQ) {
-        const int64_t qc = std::min<int64_t>(TQ, lq - qb);
-        const int64_t vis = hist + qb + qc;
-        int64_t n, sz;
-        even_split(vis, ps, mcp::kKvTile, &n, &sz);
-        const int rows = static_cast<int>(qc * G);
-        for (int h = 0; h < H; ++h) {
-          int64_t base = -1;
-          if (n > 1) {
-            base = b.part_rows;
-            b.part_rows += n * rows;
-            b.comb.push_back({s, h, static_cast<int32_t>(qb), static_cast<int32_t>(qc),
-                              static_cast<int32_t>(n), static_cast<int32_t>(base), rows, 0});
-          }
-          for (int64_t k = 0; k < n; ++k) {
-            mcp::WorkItem it;
-            it.seg = s;
-            it.kv_head = static_cast<int16_t>(h);
-            it.kind = mcp::kPrefillItem;
-            it.num_heads = 1;
-            it.q_begin = static_cast<int32_t>(qb);
-            it.q_count = static_cast<int32_t>(qc);
-            it.kv_begin = static_cast<int32_t>(k * sz);
-            it.kv_end = static_cast<int32_t>(std::min(vis, (k + 1) * sz));
-            it.part_row = static_cast<int32_t>(n > 1 ? base + k * rows : -1);
-            it.part_head_stride = 0;
-            const double tiles = static_cast<double>(cdiv(it.kv_end - it.kv_begin, mcp::kKvTile));
-            // tiles reading the same K/V (same segment, kv head, split) share a group
-            const int64_t gid = (static_cast<int64_t>(s) * H + h) * 4096 + k;
-            pre.push_back({it, 300.0 + tiles * 4.0 * 128 * 128 * d.head_dim / 6000.0, gid});
-          }
+      int64_t n, sz;
+      even_split(vis, ps, mcp::kKvTile, &n, &sz);
+      for (int h = 0; h < H; ++h) {
+        int64_t base = -1;
+        if (n > 1) {
+          base = b.part_rows;
+          b.part_rows += n * rows_n;
+          b.comb.push_back({s, h, static_cast<int32_t>(x.qb), static_cast<int32_t>(x.qc),
+                            static_cast<int32_t>(n), static_cast<int32_t>(base), rows_n, 0});
+        }
+        for (int64_t k = 0; k < n; ++k) {
+          mcp::WorkItem it;
+          it.seg = s;
+          it.kv_head = static_cast<int16_t>(h);
+          it.kind = mcp::kPrefillItem;
+          it.num_heads = 1;
+          it.q_begin = static_cast<int32_t>(x.qb);
+          it.q_count = static_cast<int32_t>(x.qc);
+          it.kv_begin = static_cast<int32_t>(k * sz);
+          it.kv_end = static_cast<int32_t>(std::min(vis, (k + 1) * sz));
+          it.part_row = static_cast<int32_t>(n > 1 ? base + k * rows_n : -1);
+          it.part_head_stride = 0;
+          const double tiles = static_cast<double>(cdiv(it.kv_end - it.kv_begin, mcp::kKvTile));
+          // tiles reading the same K/V (same segment, kv head, split) share a group
+          const int64_t gid = (static_cast<int64_t>(s) * H + h) * 4096 + k;
+          pre.push_back({it, 300.0 + tiles * 4.0 * 128 * 128 * d.head_dim / 6000.0, gid});
         }
       }
     }
@@ -400,7 +437,8 @@ namespace {
 // Validate, build the work lists and fill *plan (no device access unless the
 // SM count has to be queried).
 mcp_status plan_common(const mcp_attn_desc* desc, const int32_t* cu, const int32_t* sk,
-                       const mcp_plan_options* opts, mcp_plan* plan, Built& b) {
+                       const mcp_plan_options* opts, mcp_plan* plan, Built& b,
+                       const int32_t* rows = nullptr, int32_t num_rows = 0) {
   mcp_status st = validate_desc(desc);
   if (st != MCP_OK) return st;
   if (!plan) return fail(MCP_ERR_INVALID_ARG, "plan is NULL");
@@ -412,6 +450,16 @@ mcp_status plan_common(const mcp_attn_desc* desc, const int32_t* cu, const int32
   }
   st = validate_meta(desc->num_seqs, desc->total_q, desc->page_size, desc->max_pages_per_seq, cu, sk);
   if (st != MCP_OK) return st;
+  if (rows) {
+    if (num_rows < 0) return fail(MCP_ERR_INVALID_ARG, "num_rows %d < 0", num_rows);
+    for (int32_t i = 0; i < num_rows; ++i) {
+      if (rows[i] < 0 || rows[i] >= desc->total_q)
+        return fail(MCP_ERR_INVALID_ARG, "rows[%d] = %d outside [0, %d)", i, rows[i], desc->total_q);
+      if (i > 0 && rows[i] <= rows[i - 1])
+        return fail(MCP_ERR_INVALID_ARG, "rows must be strictly increasing (rows[%d] = %d)", i,
+                    rows[i]);
+    }
+  }
   int num_sms = opts ? opts->num_sms : 0;
   if (num_sms <= 0) {
     int dev = 0;
@@ -419,7 +467,7 @@ mcp_status plan_common(const mcp_attn_desc* desc, const int32_t* cu, const int32
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(MCP_ERR_CUDA, "SM count query: %s", cudaGetErrorString(e));
   }
-  build(*desc, cu, sk, num_sms, opts, b);
+  build(*desc, cu, sk, num_sms, opts, b, rows, num_rows);
   if (b.part_rows > INT32_MAX || static_cast<int64_t>(b.items.size()) > INT32_MAX)
     return fail(MCP_ERR_UNSUPPORTED, "step too large for one plan");
   mcp_plan pl;
@@ -492,6 +540,102 @@ mcp_status mcp_mixed_attn_plan(const mcp_attn_desc* desc, const int32_t* h_cu_se
   } catch (...) {
     return fail(MCP_ERR_INVALID_ARG, "unexpected host error while planning");
   }
+}
+
+mcp_status mcp_mixed_attn_plan_rows(const mcp_attn_desc* desc, const int32_t* h_cu_seqlens_q,
+                                    const int32_t* h_seqlens_k, const int32_t* h_rows,
+                                    int32_t num_rows, const mcp_plan_options* opts,
+                                    mcp_plan* plan, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  if (!h_rows && num_rows > 0) return fail(MCP_ERR_INVALID_ARG, "rows is NULL");
+  static const int32_t kNone = 0;
+  try {
+    Built b;
+    mcp_status st = plan_common(desc, h_cu_seqlens_q, h_seqlens_k, opts, plan, b,
+                                h_rows ? h_rows : &kNone, num_rows);
+    if (st != MCP_OK) return st;
+    const mcp_plan& pl = *plan;
+    if (!workspace) return okay();
+    if (!aligned(workspace, 256)) return fail(MCP_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    if (static_cast<int64_t>(workspace_bytes) < pl.workspace_bytes)
+      return fail(MCP_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %lld needed", workspace_bytes,
+                  static_cast<long long>(pl.workspace_bytes));
+    const size_t nbytes = static_cast<size_t>(pl.off_part_o);
+    g_staging.resize(nbytes);
+    write_lists(pl, b, g_staging.data());
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (nbytes > 0)
+      e = cudaMemcpyAsync(workspace, g_staging.data(), nbytes, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(static_cast<char*>(workspace) + pl.off_error, 0, 256, cs);
+    if (e != cudaSuccess) return fail(MCP_ERR_CUDA, "plan upload: %s", cudaGetErrorString(e));
+    return okay();
+  } catch (const std::bad_alloc&) {
+    return fail(MCP_ERR_INVALID_ARG, "host allocation failed while planning");
+  } catch (...) {
+    return fail(MCP_ERR_INVALID_ARG, "unexpected host error while planning");
+  }
+}
+
+mcp_status mcp_mixed_attn_plan_rows_host(const mcp_attn_desc* desc, const int32_t* h_cu_seqlens_q,
+                                         const int32_t* h_seqlens_k, const int32_t* h_rows,
+                                         int32_t num_rows, const mcp_plan_options* opts,
+                                         mcp_plan* plan, void* host_buffer, size_t host_bytes) {
+  if (!h_rows && num_rows > 0) return fail(MCP_ERR_INVALID_ARG, "rows is NULL");
+  static const int32_t kNone = 0;
+  try {
+    Built b;
+    mcp_status st = plan_common(desc, h_cu_seqlens_q, h_seqlens_k, opts, plan, b,
+                                h_rows ? h_rows : &kNone, num_rows);
+    if (st != MCP_OK) return st;
+    if (!host_buffer) return okay();
+    if (static_cast<int64_t>(host_bytes) < plan->off_part_o)
+      return fail(MCP_ERR_WORKSPACE_TOO_SMALL, "host buffer %zu bytes < %lld needed", host_bytes,
+                  static_cast<long long>(plan->off_part_o));
+    write_lists(*plan, b, static_cast<unsigned char*>(host_buffer));
+    return okay();
+  } catch (const std::bad_alloc&) {
+    return fail(MCP_ERR_INVALID_ARG, "host allocation failed while planning");
+  } catch (...) {
+    return fail(MCP_ERR_INVALID_ARG, "unexpected host error while planning");
+  }
+}
+
+mcp_status mcp_build_logits_indices(int32_t num_seqs, const int32_t* h_cu_seqlens_q,
+                                    const uint8_t* h_sample_mask, int32_t* h_out, int32_t* count) {
+  if (num_seqs < 0) return fail(MCP_ERR_INVALID_ARG, "num_seqs %d < 0", num_seqs);
+  if (!h_cu_seqlens_q || !count || (num_seqs > 0 && !h_out))
+    return fail(MCP_ERR_INVALID_ARG, "NULL pointer argument");
+  if (h_cu_seqlens_q[0] != 0)
+    return fail(MCP_ERR_INVALID_ARG, "cu_seqlens_q[0] = %d, expected 0", h_cu_seqlens_q[0]);
+  int32_t n = 0;
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    const int32_t lo = h_cu_seqlens_q[s], hi = h_cu_seqlens_q[s + 1];
+    if (hi < lo) return fail(MCP_ERR_INVALID_ARG, "cu_seqlens_q decreases at segment %d", s);
+    if (hi == lo) continue;  // no token this step: nothing to sample
+    if (h_sample_mask && !h_sample_mask[s]) continue;
+    h_out[n++] = hi - 1;
+  }
+  *count = n;
+  return okay();
+}
+
+mcp_status mcp_gather_rows(const void* src, int32_t num_src_rows, int32_t row_bytes,
+                           const int32_t* rows, int32_t num_rows, void* dst, int32_t* error_word,
+                           void* stream) {
+  if (num_src_rows < 0 || num_rows < 0 || row_bytes <= 0)
+    return fail(MCP_ERR_INVALID_ARG, "bad sizes (src rows %d, rows %d, row bytes %d)",
+                num_src_rows, num_rows, row_bytes);
+  if (row_bytes % 16 != 0) return fail(MCP_ERR_INVALID_ARG, "row_bytes %d not a multiple of 16", row_bytes);
+  if (num_rows == 0) return okay();
+  if (!src || !rows || !dst) return fail(MCP_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(src, 16) || !aligned(dst, 16) || !aligned(rows, 4))
+    return fail(MCP_ERR_INVALID_ARG, "src / dst must be 16-byte aligned");
+  const int e = mcp::launch_gather_rows(src, num_src_rows, row_bytes, rows, num_rows, dst,
+                                        error_word, stream);
+  if (e != 0) return cuda_fail(e, "gather_rows launch");
+  return okay();
 }
 
 mcp_status mcp_mixed_attn_plan_host(const mcp_attn_desc* desc, const int32_t* h_cu_seqlens_q,

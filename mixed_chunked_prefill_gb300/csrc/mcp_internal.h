@@ -84,6 +84,9 @@ int launch_append(const void* k_new, const void* v_new, const int64_t* slot_mapp
                   int32_t num_tokens, int32_t row_bytes, int64_t num_slots, void* k_cache,
                   void* v_cache, int32_t* error_word, void* stream);
 int launch_mixed_attn(const FwdArgs& a, void* stream);
+int launch_gather_rows(const void* src, int32_t num_src_rows, int32_t row_bytes,
+                       const int32_t* rows, int32_t num_rows, void* dst, int32_t* error_word,
+                       void* stream);
 int launch_combine(const FwdArgs& a, void* stream);
 int launch_merge_states(const float* o_parts, const float* lse_parts, int32_t n, int32_t rows,
                         int32_t heads, int32_t head_dim, void* out, float* lse_out, void* stream);

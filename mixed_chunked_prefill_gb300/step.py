@@ -22,6 +22,7 @@ from . import (
     make_desc,
     mixed_attn_fwd,
     mixed_attn_plan,
+    mixed_attn_plan_rows,
     paged_kv_append,
     workspace_error_word,
 )
@@ -36,7 +37,9 @@ class MixedStep:
 
     def __init__(self, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, sm_scale,
                  cu_seqlens_q, seqlens_k, block_tables, device="cuda", options=None,
-                 stream=None):
+                 stream=None, rows=None):
+        """``rows``: None for every query row, else the token indices (e.g.
+        logits_indices) whose attention rows this step computes."""
         import torch
 
         self.cu_h = _i32(cu_seqlens_q)
@@ -55,11 +58,19 @@ class MixedStep:
         self.sk_d = torch.from_numpy(self.sk_h).to(device)
         self.bt_d = torch.from_numpy(self.bt_h).to(device)
         self.slots_d = torch.from_numpy(self.slots_h).to(device)
-        sizing = mixed_attn_plan(self.desc, self.cu_h, self.sk_h, options)
+        if rows is None:
+            def planner(ws=None, st=None):
+                return mixed_attn_plan(self.desc, self.cu_h, self.sk_h, options, ws, st)
+        else:
+            self.rows_h = _i32(rows)
+
+            def planner(ws=None, st=None):
+                return mixed_attn_plan_rows(self.desc, self.cu_h, self.sk_h, self.rows_h,
+                                            options, ws, st)
+        sizing = planner()
         self.workspace = torch.empty(max(256, int(sizing.workspace_bytes)), dtype=torch.uint8,
                                      device=device)
-        self.plan = mixed_attn_plan(self.desc, self.cu_h, self.sk_h, options, self.workspace,
-                                    stream)
+        self.plan = planner(self.workspace, stream)
         self.error_word = workspace_error_word(self.plan, self.workspace)
 
     def append(self, k_new, v_new, k_cache, v_cache):

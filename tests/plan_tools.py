@@ -42,3 +42,25 @@ def plan_host(desc, cu, sk, num_sms=152, dsplit=0, psplit=0):
     items = buf[:plan.num_items * 32].view(ITEM).copy()
     comb = buf[plan.off_combine:plan.off_combine + plan.num_combine * 32].view(COMB).copy()
     return st, plan, items, comb
+
+
+def plan_rows_host(desc, cu, sk, rows, num_sms=152, dsplit=0, psplit=0):
+    """(status, plan, items, combine) from mcp_mixed_attn_plan_rows_host."""
+    lib = mcp.load()
+    cu = np.ascontiguousarray(np.asarray(cu, dtype=np.int32))
+    sk = np.ascontiguousarray(np.asarray(sk, dtype=np.int32))
+    rw = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    opts = mcp.PlanOptions(num_sms, dsplit, psplit)
+    plan = mcp.Plan()
+    args = (ctypes.byref(desc), cu.ctypes.data_as(ctypes.c_void_p),
+            sk.ctypes.data_as(ctypes.c_void_p), rw.ctypes.data_as(ctypes.c_void_p), int(rw.size),
+            ctypes.byref(opts), ctypes.byref(plan))
+    st = lib.mcp_mixed_attn_plan_rows_host(*args, None, 0)
+    if st != _capi.MCP_OK:
+        return st, None, None, None
+    buf = np.zeros(max(1, int(plan.off_part_o)), dtype=np.uint8)
+    st = lib.mcp_mixed_attn_plan_rows_host(*args, buf.ctypes.data_as(ctypes.c_void_p), buf.size)
+    assert st == _capi.MCP_OK
+    items = buf[:plan.num_items * 32].view(ITEM).copy()
+    comb = buf[plan.off_combine:plan.off_combine + plan.num_combine * 32].view(COMB).copy()
+    return st, plan, items, comb
