@@ -41,12 +41,25 @@ L2_FLUSH_BYTES = 256 << 20
 # algorithmic work of one step (what the method must move / compute)
 # ---------------------------------------------------------------------------
 
-def algorithmic(w):
+def algorithmic(w, rows=None):
     """Bytes and tensor FLOPs of one step, per the roofline definition: every
     KV position read once per kv head (K and V), Q read and O written once;
     the append reads and writes the new rows; tensor FLOPs are the visible
-    (query, key) pairs of the chunk segments x 2 matmuls x 2 flops x D x H_q."""
+    (query, key) pairs of the chunk segments x 2 matmuls x 2 flops x D x H_q.
+    With ``rows`` (token indices) only those query rows are computed: the KV a
+    listed token sees, read once per kv head, and its Q / O rows."""
     D, Hq, Hkv = w.head_dim, w.num_q_heads, w.num_kv_heads
+    if rows is not None:
+        cu = np.concatenate([[0], np.cumsum(w.q_lens)])
+        seg = np.searchsorted(cu, rows, side="right") - 1
+        vis = {}
+        for t, s in zip(rows, seg):  # a segment's KV is read up to its last listed token
+            vis[s] = max(vis.get(s, 0), w.k_lens[s] - w.q_lens[s] + int(t - cu[s]) + 1)
+        kv_bytes = sum(vis.values()) * Hkv * D * 2 * 2
+        qo = len(rows) * Hq * D * 2
+        append_bytes = w.total_q * Hkv * D * 2 * 2 * 2
+        return dict(kv_bytes=kv_bytes, q_bytes=qo, o_bytes=qo, append_bytes=append_bytes,
+                    fwd_bytes=kv_bytes + 2 * qo, flops_tc=0, flops_dec=0)
     kv_bytes = sum(w.k_lens[s] for s in range(w.num_seqs) if w.q_lens[s] > 0) * Hkv * D * 2 * 2
     q_bytes = w.total_q * Hq * D * 2
     o_bytes = w.total_q * Hq * D * 2
@@ -169,7 +182,9 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     w = synth.make_workload(args.config)
-    alg = algorithmic(w)
+    cu0 = np.concatenate([[0], np.cumsum(w.q_lens)]).astype(np.int32)
+    rows = mcp.build_logits_indices(cu0) if args.rows == "logits" else None
+    alg = algorithmic(w, rows)
     peaks = load_peaks()
 
     with torch.cuda.stream(stream):
@@ -184,7 +199,7 @@ def run_gpu(args, rank, world, local_rank):
         cu = np.concatenate([[0], np.cumsum(w.q_lens)]).astype(np.int32)
         t0 = time.perf_counter()
         step = MixedStep(w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size, w.num_pages,
-                         w.sm_scale, cu, w.k_lens, bt, device=dev, stream=stream)
+                         w.sm_scale, cu, w.k_lens, bt, device=dev, stream=stream, rows=rows)
         plan_us = (time.perf_counter() - t0) * 1e6
         q, k_new, v_new = t["q"], t["k_new"], t["v_new"]
         out = torch.empty_like(q)
@@ -235,7 +250,7 @@ def run_gpu(args, rank, world, local_rank):
 
     # end to end through the C ABI from pinned host buffers
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and rows is None:
         q_h = q.cpu().pin_memory()
         k_h = k_new.cpu().pin_memory()
         v_h = v_new.cpu().pin_memory()
@@ -292,6 +307,8 @@ def run_gpu(args, rank, world, local_rank):
                    "kv_tokens": int(sum(w.k_lens)), "l2": "flushed between steps (256 MB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "step": "paged_kv_append + mixed_attn_fwd (+ combine)",
+                   "rows": ("all" if rows is None else
+                            f"logits_indices only ({len(rows)} of {w.total_q} query rows)"),
                    "work_items": int(step.plan.num_items),
                    "decode_items": int(step.plan.num_decode_items),
                    "prefill_items": int(step.plan.num_prefill_items),
@@ -418,6 +435,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", default="all", choices=["all", "logits"],
+                    help="logits: attention only for logits_indices (the last layer's rows)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -438,7 +457,7 @@ def main():
         torch.distributed.init_process_group("nccl")
     res = run_gpu(args, rank, world, local_rank)
     if rank == 0:
-        if not args.no_cpu_baseline and world == 1:
+        if not args.no_cpu_baseline and world == 1 and args.rows == "all":
             res["cpu_baseline"] = cpu_baseline(args.config)
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -195,7 +195,12 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
   };
 
   // Decode splits: about eight decode items per SM (each item streams its KV
-  // range for a whole kv-head group), never below 1024 tokens.
+  // range for a whole kv-head group), not below 1024 tokens -- or 256 when the
+  // step has no tensor-core tiles, so that a few long rows alone (e.g. the
+  // sampled rows of a step) still spread over many SMs.
+  bool any_tc = false;
+  for (const Unit& x : units) any_tc = any_tc || !x.decode;
+  const int64_t ds_floor = any_tc ? 1024 : 256;
   int64_t ds;
   if (dopt > 0) {
     ds = round_up(dopt, mcp::kPageSize);
@@ -208,7 +213,7 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
   int64_t ps = popt > 0 ? round_up(popt, mcp::kKvTile) : 32768;
   while (count(ds, ps) < 2LL * num_sms) {
     bool changed = false;
-    if (dopt <= 0 && ds > 1024) { ds = std::max<int64_t>(1024, ds / 2); changed = true; }
+    if (dopt <= 0 && ds > ds_floor) { ds = std::max<int64_t>(ds_floor, ds / 2); changed = true; }
     if (popt <= 0 && ps > 2048) { ps /= 2; changed = true; }
     if (!changed) break;
   }
