@@ -382,6 +382,64 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
+def run_kv_swap(args):
+    """Swap-out / swap-in rate of KV pages between the device pool and a
+    page-locked host pool (mcp_kv_copy_pages), against a contiguous
+    page-locked cudaMemcpyAsync of the same bytes (the host link's practical
+    peak on this machine)."""
+    import torch
+
+    import mixed_chunked_prefill_gb300 as mcp
+    from mixed_chunked_prefill_gb300 import build as mcp_build
+
+    mcp_build.build()
+    mcp.load()
+    dev = torch.device("cuda", 0)
+    P, Hkv, D = 16, 8, 128
+    pool, n = 16384, 8192                       # 1 GB device pool; 512 MB (K+V) moved
+    page_bytes = 2 * P * Hkv * D * 2            # K and V of one page
+    kc = torch.zeros((pool, P, Hkv, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    hk = torch.zeros((n, P, Hkv, D), dtype=torch.bfloat16).pin_memory()
+    hv = torch.zeros_like(hk).pin_memory()
+    rng = np.random.Generator(np.random.PCG64(11))
+    dev_pages = torch.from_numpy(rng.permutation(pool)[:n].astype(np.int32)).to(dev)
+    host_slots = torch.arange(n, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn, reps=5):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps / 1e3
+
+    t_out = timed(lambda: mcp.kv_copy_pages(kc, vc, hk, hv, dev_pages, host_slots))
+    t_in = timed(lambda: mcp.kv_copy_pages(hk, hv, kc, vc, host_slots, dev_pages))
+    flat_d = kc[:n].view(-1)
+    flat_h = hk.view(-1)
+    t_d2h = timed(lambda: (flat_h.copy_(flat_d, non_blocking=True),
+                           hv.view(-1).copy_(vc[:n].view(-1), non_blocking=True)))
+    t_h2d = timed(lambda: (flat_d.copy_(flat_h, non_blocking=True),
+                           vc[:n].view(-1).copy_(hv.view(-1), non_blocking=True)))
+    moved = n * page_bytes
+    gbs = lambda t: moved / t / 1e9
+    return {"metric": "KV page swap-out / swap-in (mcp_kv_copy_pages)", "value": gbs(t_in),
+            "unit": "GB/s", "n_gpus": 1, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic (zero-filled pools, random page permutation)",
+            "config": {"workload": f"{n} random pages of {page_bytes // 1024} KB (K+V, 16 tokens "
+                                   f"x {Hkv} kv heads x {D}) between a {pool}-page device pool "
+                                   "and a page-locked host pool", "pages": n},
+            "swap_out_gbs": gbs(t_out), "swap_in_gbs": gbs(t_in),
+            "contiguous_memcpy_d2h_gbs": gbs(t_d2h), "contiguous_memcpy_h2d_gbs": gbs(t_h2d),
+            "frac_of_memcpy": {"out": t_d2h / t_out, "in": t_h2d / t_in}}
+
+
 def cpu_baseline(name, budget_s=15.0):
     s = OracleSample(name)
     rows = s.rows(4)
@@ -435,6 +493,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-swap", action="store_true",
+                    help="time KV page swap-out / swap-in instead of the step")
     ap.add_argument("--rows", default="all", choices=["all", "logits"],
                     help="logits: attention only for logits_indices (the last layer's rows)")
     args = ap.parse_args()
@@ -447,6 +507,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.kv_swap:
+        if rank == 0:
+            print(json.dumps(run_kv_swap(args)), flush=True)
         return
 
     if world > 1:

@@ -353,6 +353,31 @@ mcp_status mcp_gather_rows(const void* src, int32_t num_src_rows, int32_t row_by
                            void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* KV page copies between pools: swap-out / swap-in                          */
+/* ------------------------------------------------------------------------- */
+/*
+ * [X] m.xxqk.cn "动态批处理中的抢占与优先级调度", section "Prefill 算力霸占与抢占
+ * 策略演进": when the KV pool runs out, a preempted sequence's KV pages are
+ * copied out to host memory (swap-out) and copied back into free pages once
+ * memory is available again (swap-in).  For i < num:
+ *   k_dst[dst_pages[i]] = k_src[src_pages[i]]   (whole pages of page_bytes
+ *   v_dst[dst_pages[i]] = v_src[src_pages[i]]    bytes, bit-exact)
+ * Pools: k_src / v_src with src_num_pages pages, k_dst / v_dst with
+ * dst_num_pages pages; each pool is device memory or page-locked host memory
+ * (a swap pool), read and written by the kernel directly.  page_bytes =
+ * page_size * num_kv_heads * head_dim * 2 for the caches of this library; a
+ * multiple of 16.  src_pages, dst_pages: int32 [num], device (or page-locked
+ * host) memory.  Destination pages must be distinct; when src and dst are
+ * the same pool, no destination page may also be a source page.  A page id
+ * outside its pool skips that page and sets MCP_DEVERR_PAGE_RANGE in
+ * error_word (if not NULL).  Asynchronous on `stream`.
+ */
+mcp_status mcp_kv_copy_pages(const void* k_src, const void* v_src, int32_t src_num_pages,
+                             void* k_dst, void* v_dst, int32_t dst_num_pages, int32_t page_bytes,
+                             const int32_t* src_pages, const int32_t* dst_pages, int32_t num,
+                             int32_t* error_word, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* One step from host memory, two steps in flight                            */
 /* ------------------------------------------------------------------------- */
 /*

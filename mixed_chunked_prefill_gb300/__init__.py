@@ -28,7 +28,7 @@ __all__ = [
     "AttnDesc", "Plan", "PlanOptions", "MCPError", "load", "abi_version", "paged_kv_append",
     "build_slot_mapping", "mixed_attn_plan", "mixed_attn_fwd", "check_device_errors",
     "workspace_error_word", "merge_states", "make_desc", "mixed_attn_fwd_noalloc",
-    "mixed_attn_plan_rows", "build_logits_indices", "gather_rows",
+    "mixed_attn_plan_rows", "build_logits_indices", "gather_rows", "kv_copy_pages",
 ]
 
 
@@ -181,6 +181,41 @@ def build_logits_indices(cu_seqlens_q, sample_mask=None) -> np.ndarray:
                                       ctypes.byref(count))
     _capi.check(st, "build_logits_indices")
     return out[:count.value].copy()
+
+
+def kv_copy_pages(k_src, v_src, k_dst, v_dst, src_pages, dst_pages, error_word=None,
+                  stream=None) -> None:
+    """Copy whole KV pages between two pools ([pages, P, H_kv, D] bf16 tensors,
+    device or page-locked host): dst[dst_pages[i]] = src[src_pages[i]].
+    ``src_pages`` / ``dst_pages``: int32 tensors on the device (or pinned)."""
+    import torch
+
+    lib = load()
+    n = int(src_pages.numel())
+    if int(dst_pages.numel()) != n:
+        raise ValueError("src_pages and dst_pages differ in length")
+    for t, name in ((k_src, "k_src"), (v_src, "v_src"), (k_dst, "k_dst"), (v_dst, "v_dst")):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 page pool")
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name} must be device or page-locked host memory")
+    if tuple(k_src.shape[1:]) != tuple(k_dst.shape[1:]) or k_src.shape != v_src.shape \
+            or k_dst.shape != v_dst.shape:
+        raise ValueError("pools must have the same page shape")
+    for t, name in ((src_pages, "src_pages"), (dst_pages, "dst_pages")):
+        if t.dtype != torch.int32 or not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name} must be an int32 device (or pinned) tensor")
+    page_bytes = int(k_src[0].numel()) * 2
+    if error_word is None or isinstance(error_word, torch.Tensor):
+        ew = _dev(error_word, torch.int32, "error_word")
+    else:
+        ew = ctypes.c_void_p(int(error_word))
+    st = lib.mcp_kv_copy_pages(ctypes.c_void_p(k_src.data_ptr()), ctypes.c_void_p(v_src.data_ptr()),
+                               int(k_src.shape[0]), ctypes.c_void_p(k_dst.data_ptr()),
+                               ctypes.c_void_p(v_dst.data_ptr()), int(k_dst.shape[0]), page_bytes,
+                               ctypes.c_void_p(src_pages.data_ptr()),
+                               ctypes.c_void_p(dst_pages.data_ptr()), n, ew, _stream(stream))
+    _capi.check(st, "kv_copy_pages")
 
 
 def gather_rows(src, rows, dst, error_word=None, stream=None) -> None:

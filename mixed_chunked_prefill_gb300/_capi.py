@@ -113,6 +113,8 @@ SIGNATURES = {
     "mcp_mixed_attn_plan_rows_host": (c_int32, [POINTER(AttnDesc), c_void_p, c_void_p,
                                                 c_void_p, c_int32, POINTER(PlanOptions),
                                                 POINTER(Plan), c_void_p, c_size_t]),
+    "mcp_kv_copy_pages": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int32,
+                                    c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
     "mcp_gather_rows": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p,
                                   c_void_p, c_void_p]),
     "mcp_host_step_arena_bytes": (c_int32, [POINTER(AttnDesc), POINTER(HostStepLimits),

@@ -1,5 +1,6 @@
-// Row copies of the step: the paged KV append (scatter each new token's K/V
-// row into its physical slot) and the row gather of the sampled positions.
+// Row and page copies around the step: the paged KV append (scatter each new
+// token's K/V row into its physical slot), the row gather of the sampled
+// positions, and whole-page copies between page pools (swap-out / swap-in).
 //
 // [W] "输入组装": the new tokens' K/V are written into the paged cache through
 // slot_mapping before attention runs; [L] 4.2 (append_paged_kv_cache):
@@ -62,6 +63,32 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   }
 }
 
+// Whole-page copies between two page pools: dst[dst_pages[i]] = src[src_pages[i]]
+// for K and V.  Either pool may be page-locked host memory (swap-out / swap-in
+// of a preempted sequence's pages) or device memory (copy-on-write).  A page
+// id outside its pool is reported and that page skipped.
+__global__ void __launch_bounds__(256) copy_pages_kernel(
+    const uint4* __restrict__ k_src, const uint4* __restrict__ v_src, int32_t src_pages_total,
+    uint4* __restrict__ k_dst, uint4* __restrict__ v_dst, int32_t dst_pages_total,
+    const int32_t* __restrict__ src_pages, const int32_t* __restrict__ dst_pages,
+    int64_t total_vec, int32_t vec_per_page, int32_t* err) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vec;
+       i += stride) {
+    const int64_t p = i / vec_per_page;
+    const int64_t c = i - p * vec_per_page;
+    const int32_t sp = src_pages[p], dp = dst_pages[p];
+    if (sp < 0 || sp >= src_pages_total || dp < 0 || dp >= dst_pages_total) {
+      if (err && c == 0) atomicOr(err, MCP_DEVERR_PAGE_RANGE);
+      continue;
+    }
+    const int64_t from = static_cast<int64_t>(sp) * vec_per_page + c;
+    const int64_t to = static_cast<int64_t>(dp) * vec_per_page + c;
+    k_dst[to] = k_src[from];
+    v_dst[to] = v_src[from];
+  }
+}
+
 int grid_for(int64_t total) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -82,6 +109,20 @@ int launch_gather_rows(const void* src, int32_t num_src_rows, int32_t row_bytes,
   gather_rows_kernel<<<grid_for(total), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(src), num_src_rows, rows, total, vec, static_cast<uint4*>(dst),
       error_word);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_copy_pages(const void* k_src, const void* v_src, int32_t src_num_pages, void* k_dst,
+                      void* v_dst, int32_t dst_num_pages, int32_t page_bytes,
+                      const int32_t* src_pages, const int32_t* dst_pages, int32_t num,
+                      int32_t* error_word, void* stream) {
+  if (num <= 0) return 0;
+  const int32_t vec = page_bytes / 16;
+  const int64_t total = static_cast<int64_t>(num) * vec;
+  copy_pages_kernel<<<grid_for(total), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k_src), static_cast<const uint4*>(v_src), src_num_pages,
+      static_cast<uint4*>(k_dst), static_cast<uint4*>(v_dst), dst_num_pages, src_pages, dst_pages,
+      total, vec, error_word);
   return static_cast<int>(cudaGetLastError());
 }
 

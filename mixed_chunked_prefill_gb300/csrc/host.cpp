@@ -626,6 +626,26 @@ mcp_status mcp_build_logits_indices(int32_t num_seqs, const int32_t* h_cu_seqlen
   return okay();
 }
 
+mcp_status mcp_kv_copy_pages(const void* k_src, const void* v_src, int32_t src_num_pages,
+                             void* k_dst, void* v_dst, int32_t dst_num_pages, int32_t page_bytes,
+                             const int32_t* src_pages, const int32_t* dst_pages, int32_t num,
+                             int32_t* error_word, void* stream) {
+  if (num < 0 || src_num_pages < 0 || dst_num_pages < 0 || page_bytes <= 0)
+    return fail(MCP_ERR_INVALID_ARG, "bad sizes (num %d, pools %d / %d, page bytes %d)", num,
+                src_num_pages, dst_num_pages, page_bytes);
+  if (page_bytes % 16 != 0)
+    return fail(MCP_ERR_INVALID_ARG, "page_bytes %d not a multiple of 16", page_bytes);
+  if (num == 0) return okay();
+  if (!k_src || !v_src || !k_dst || !v_dst || !src_pages || !dst_pages)
+    return fail(MCP_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(k_src, 16) || !aligned(v_src, 16) || !aligned(k_dst, 16) || !aligned(v_dst, 16))
+    return fail(MCP_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+  const int e = mcp::launch_copy_pages(k_src, v_src, src_num_pages, k_dst, v_dst, dst_num_pages,
+                                       page_bytes, src_pages, dst_pages, num, error_word, stream);
+  if (e != 0) return cuda_fail(e, "kv_copy_pages launch");
+  return okay();
+}
+
 mcp_status mcp_gather_rows(const void* src, int32_t num_src_rows, int32_t row_bytes,
                            const int32_t* rows, int32_t num_rows, void* dst, int32_t* error_word,
                            void* stream) {

@@ -84,6 +84,10 @@ int launch_append(const void* k_new, const void* v_new, const int64_t* slot_mapp
                   int32_t num_tokens, int32_t row_bytes, int64_t num_slots, void* k_cache,
                   void* v_cache, int32_t* error_word, void* stream);
 int launch_mixed_attn(const FwdArgs& a, void* stream);
+int launch_copy_pages(const void* k_src, const void* v_src, int32_t src_num_pages, void* k_dst,
+                      void* v_dst, int32_t dst_num_pages, int32_t page_bytes,
+                      const int32_t* src_pages, const int32_t* dst_pages, int32_t num,
+                      int32_t* error_word, void* stream);
 int launch_gather_rows(const void* src, int32_t num_src_rows, int32_t row_bytes,
                        const int32_t* rows, int32_t num_rows, void* dst, int32_t* error_word,
                        void* stream);

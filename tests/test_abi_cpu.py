@@ -330,3 +330,15 @@ def test_planner_balance_bound_big_configs():
         makespan = max(sms)
         lower = max(cost.sum() / 152, cost.max())
         assert makespan <= 1.1 * lower, (name, makespan / lower)
+
+
+def test_kv_copy_pages_validation_before_launch():
+    lib = mcp.load()
+    p = ctypes.c_void_p(0x1000)
+    # page_bytes not a multiple of 16, negative sizes, NULLs, misaligned pools
+    assert lib.mcp_kv_copy_pages(p, p, 4, p, p, 4, 24, p, p, 1, None, None) == 1
+    assert lib.mcp_kv_copy_pages(p, p, -1, p, p, 4, 32, p, p, 1, None, None) == 1
+    assert lib.mcp_kv_copy_pages(None, p, 4, p, p, 4, 32, p, p, 1, None, None) == 1
+    assert lib.mcp_kv_copy_pages(ctypes.c_void_p(0x1008), p, 4, p, p, 4, 32, p, p, 1, None,
+                                 None) == 1
+    assert lib.mcp_kv_copy_pages(None, None, 0, None, None, 0, 32, None, None, 0, None, None) == 0
