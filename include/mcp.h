@@ -378,6 +378,85 @@ mcp_status mcp_kv_copy_pages(const void* k_src, const void* v_src, int32_t src_n
                              int32_t* error_word, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* Step builder: the chunked-prefill scheduler (host-only)                   */
+/* ------------------------------------------------------------------------- */
+/*
+ * Decides, step by step, which requests run and with how many tokens, and
+ * builds the step's metadata.  [W] wangyu.me sections "Token 预算：
+ * max_num_batched_tokens" and "调度器：running 优先，waiting 填充": each request
+ * tracks num_computed_tokens; a step has a token budget; running requests go
+ * first (decodes and unfinished prompts, in arrival order), then waiting
+ * requests fill what is left, a prompt taking as many tokens as the budget
+ * allows; long_prefill_token_threshold (0 = none) caps one chunk, for running
+ * and newly admitted prompts alike.
+ * [W] "采样": the step's logits_indices are the last token of every segment;
+ * only decodes and chunks that finish their prompt sample.  [X] m.xxqk.cn
+ * "动态批处理中的抢占与优先级调度": waiting requests are admitted by priority
+ * (higher first, then arrival); when the KV page pool cannot hold a running
+ * request's next tokens, the lowest-priority, latest-arrived running request
+ * is preempted -- recomputed (its pages are freed and it re-enters the
+ * waiting queue with all its tokens as prompt) or swapped (its pages are
+ * listed for swap-out to host pool pages and swapped back in, into free
+ * device pages, when it resumes).  Page 16-token granularity, one page table
+ * row per request.  The object and its arrays live in host memory.
+ */
+typedef struct mcp_sched_config {
+  int32_t max_num_batched_tokens;       /* token budget of one step (>= 1)           */
+  int32_t long_prefill_token_threshold; /* 0 = none, else max tokens of one chunk    */
+  int32_t max_num_seqs;                 /* segments in one step (>= 1)               */
+  int32_t num_pages;                    /* device KV pool pages                      */
+  int32_t page_size;                    /* tokens per page (16)                      */
+  int32_t max_pages_per_seq;            /* block-table row length                    */
+  int32_t preempt_swap;                 /* 0 = recompute, 1 = swap to the host pool  */
+  int32_t num_host_pages;               /* host swap pool pages (swap mode)          */
+  int32_t reserved[4];                  /* must be 0                                 */
+} mcp_sched_config;
+
+typedef struct mcp_sched mcp_sched; /* opaque */
+
+/* One step's plan.  Arrays are owned by the scheduler and stay valid until
+ * the next mcp_sched_schedule() / mcp_sched_destroy().  Execute the step as:
+ * swap-out copies, swap-in copies, then append + attention with the arrays. */
+typedef struct mcp_sched_output {
+  int32_t num_seqs;            /* segments of the step (0 = nothing runnable)      */
+  int32_t total_q;             /* tokens of the step                               */
+  const int64_t* request_ids;  /* [num_seqs]                                       */
+  const int32_t* cu_seqlens_q; /* [num_seqs + 1]                                   */
+  const int32_t* seqlens_k;    /* [num_seqs]: tokens in the cache after the step   */
+  const int32_t* block_tables; /* [num_seqs, max_pages_per_seq], -1 padded         */
+  const uint8_t* sample_mask;  /* [num_seqs]: 1 = the segment samples a token      */
+  const int32_t* logits_indices; /* [num_logits]: last token of sampling segments  */
+  int32_t num_logits;
+  int32_t num_swap_out;        /* device page -> host page copies, before the step */
+  const int32_t* swap_out_device_pages;
+  const int32_t* swap_out_host_pages;
+  int32_t num_swap_in;         /* host page -> device page copies, before the step */
+  const int32_t* swap_in_host_pages;
+  const int32_t* swap_in_device_pages;
+  int32_t num_preempted;       /* requests preempted while building this step      */
+  const int64_t* preempted_ids;
+  int32_t reserved[4];
+} mcp_sched_output;
+
+mcp_status mcp_sched_create(const mcp_sched_config* config, mcp_sched** sched);
+/* Queue a request: a prompt of prompt_len tokens, then up to max_new_tokens
+ * sampled tokens; ids must be unique among live requests. */
+mcp_status mcp_sched_add_request(mcp_sched* sched, int64_t request_id, int32_t prompt_len,
+                                 int32_t max_new_tokens, int32_t priority);
+/* Build the next step (out receives views of the scheduler's arrays). */
+mcp_status mcp_sched_schedule(mcp_sched* sched, mcp_sched_output* out);
+/* The last scheduled step ran: advance num_computed_tokens, add one sampled
+ * token to every sampling segment, retire requests that reached
+ * max_new_tokens (their pages return to the pool).  *num_finished (if not
+ * NULL) receives how many finished; their ids go to finished_ids (if not
+ * NULL, room for num_seqs ids). */
+mcp_status mcp_sched_finish_step(mcp_sched* sched, int32_t* num_finished, int64_t* finished_ids);
+/* Counts: waiting, running, swapped, finished requests; free device pages. */
+mcp_status mcp_sched_stats(const mcp_sched* sched, int32_t* waiting, int32_t* running,
+                           int32_t* swapped, int64_t* finished, int32_t* free_pages);
+mcp_status mcp_sched_destroy(mcp_sched* sched);
+
+/* ------------------------------------------------------------------------- */
 /* One step from host memory, two steps in flight                            */
 /* ------------------------------------------------------------------------- */
 /*

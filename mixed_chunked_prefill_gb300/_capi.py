@@ -68,6 +68,43 @@ class Plan(ctypes.Structure):
     ]
 
 
+class SchedConfig(ctypes.Structure):
+    _fields_ = [
+        ("max_num_batched_tokens", c_int32),
+        ("long_prefill_token_threshold", c_int32),
+        ("max_num_seqs", c_int32),
+        ("num_pages", c_int32),
+        ("page_size", c_int32),
+        ("max_pages_per_seq", c_int32),
+        ("preempt_swap", c_int32),
+        ("num_host_pages", c_int32),
+        ("reserved", c_int32 * 4),
+    ]
+
+
+class SchedOutput(ctypes.Structure):
+    _fields_ = [
+        ("num_seqs", c_int32),
+        ("total_q", c_int32),
+        ("request_ids", POINTER(c_int64)),
+        ("cu_seqlens_q", POINTER(c_int32)),
+        ("seqlens_k", POINTER(c_int32)),
+        ("block_tables", POINTER(c_int32)),
+        ("sample_mask", POINTER(ctypes.c_uint8)),
+        ("logits_indices", POINTER(c_int32)),
+        ("num_logits", c_int32),
+        ("num_swap_out", c_int32),
+        ("swap_out_device_pages", POINTER(c_int32)),
+        ("swap_out_host_pages", POINTER(c_int32)),
+        ("num_swap_in", c_int32),
+        ("swap_in_host_pages", POINTER(c_int32)),
+        ("swap_in_device_pages", POINTER(c_int32)),
+        ("num_preempted", c_int32),
+        ("preempted_ids", POINTER(c_int64)),
+        ("reserved", c_int32 * 4),
+    ]
+
+
 class HostStepLimits(ctypes.Structure):
     _fields_ = [
         ("max_tokens", c_int32),
@@ -117,6 +154,13 @@ SIGNATURES = {
                                     c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
     "mcp_gather_rows": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p,
                                   c_void_p, c_void_p]),
+    "mcp_sched_create": (c_int32, [POINTER(SchedConfig), POINTER(c_void_p)]),
+    "mcp_sched_add_request": (c_int32, [c_void_p, c_int64, c_int32, c_int32, c_int32]),
+    "mcp_sched_schedule": (c_int32, [c_void_p, POINTER(SchedOutput)]),
+    "mcp_sched_finish_step": (c_int32, [c_void_p, POINTER(c_int32), c_void_p]),
+    "mcp_sched_stats": (c_int32, [c_void_p, POINTER(c_int32), POINTER(c_int32), POINTER(c_int32),
+                                  POINTER(c_int64), POINTER(c_int32)]),
+    "mcp_sched_destroy": (c_int32, [c_void_p]),
     "mcp_host_step_arena_bytes": (c_int32, [POINTER(AttnDesc), POINTER(HostStepLimits),
                                             POINTER(c_size_t), POINTER(c_size_t)]),
     "mcp_host_step_create": (c_int32, [POINTER(AttnDesc), POINTER(HostStepLimits), c_void_p,

@@ -22,7 +22,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmcp.so")
 
-SOURCES = ["host.cpp", "append.cu", "attn_fwd.cu", "combine.cu", "attn_fwd_noalloc.cu"]
+SOURCES = ["host.cpp", "sched.cpp", "append.cu", "attn_fwd.cu", "combine.cu",
+           "attn_fwd_noalloc.cu"]
 HEADERS = ["mcp_internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

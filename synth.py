@@ -208,3 +208,31 @@ def bf16_bits(t) -> np.ndarray:
     import torch
 
     return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _splitmix64(x: np.ndarray) -> np.ndarray:
+    """SplitMix64 finaliser (Steele, Lea, Flood 2014) on uint64 arrays."""
+    x = (x + np.uint64(0x9E3779B97F4A7C15)) & np.uint64(0xFFFFFFFFFFFFFFFF)
+    x = ((x ^ (x >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)) & np.uint64(0xFFFFFFFFFFFFFFFF)
+    x = ((x ^ (x >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)) & np.uint64(0xFFFFFFFFFFFFFFFF)
+    return x ^ (x >> np.uint64(31))
+
+
+def token_values(request_ids, positions, heads: int, dim: int, tag: int):
+    """Synthetic per-token rows for serving loops: a bf16 torch tensor
+    [n, heads, dim] whose row i depends only on (request_ids[i], positions[i],
+    tag) -- so a token recomputed after preemption, or cut into a different
+    chunk, gets exactly the same values.  Values: uniform in [-2, 2) from a
+    counter-based hash (SplitMix64), rounded to bf16."""
+    import torch
+
+    r = np.asarray(request_ids, dtype=np.uint64)[:, None, None]
+    p = np.asarray(positions, dtype=np.uint64)[:, None, None]
+    h = np.arange(heads, dtype=np.uint64)[None, :, None]
+    d = np.arange(dim, dtype=np.uint64)[None, None, :]
+    with np.errstate(over="ignore"):
+        key = (((r * np.uint64(1000003) + p) * np.uint64(8191) + h) * np.uint64(1021) + d)
+        key = key * np.uint64(16) + np.uint64(tag)
+        bits = _splitmix64(key)
+    u = (bits >> np.uint64(40)).astype(np.float64) / float(1 << 24)  # [0, 1)
+    return torch.from_numpy((4.0 * u - 2.0).astype(np.float32)).to(torch.bfloat16)
