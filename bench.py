@@ -440,6 +440,76 @@ def run_kv_swap(args):
             "frac_of_memcpy": {"out": t_d2h / t_out, "in": t_h2d / t_in}}
 
 
+def run_serve(args):
+    """Step-time distribution of a serving loop with and without chunked
+    prefill ([W] "Token 预算", [X] "Chunked Prefill 的核心算法思想"): 32 requests
+    decoding over 4096-token contexts while 8192-token prompts arrive every 50
+    steps; each step (schedule, copy-in, append + attention, copy-out) is
+    timed by wall clock after its outputs reach host memory."""
+    import torch
+
+    import mixed_chunked_prefill_gb300 as mcp
+    from mixed_chunked_prefill_gb300 import build as mcp_build
+    from mixed_chunked_prefill_gb300.serve import ServeLoop
+
+    mcp_build.build()
+    mcp.load()
+    Hq, Hkv, D = 32, 8, 128
+    n_dec, ctx, long_prompt, every, steps = 32, 4096, 8192, 50, 200
+    new_tokens = 1000  # outlasts the untimed warm-up (prompts of the decodes) + timed steps
+    pages = (n_dec * (ctx + new_tokens + 16) + 8 * (long_prompt + 16)) // 16 + 64
+    mp = (max(long_prompt, ctx + new_tokens) + 16) // 16 + 1
+    gen = torch.Generator().manual_seed(5)
+    cap = long_prompt + n_dec + 64
+    qb = torch.randn((cap, Hq, D), generator=gen).to(torch.bfloat16).pin_memory()
+    kb = torch.randn((cap, Hkv, D), generator=gen).to(torch.bfloat16).pin_memory()
+    vb = torch.randn((cap, Hkv, D), generator=gen).to(torch.bfloat16).pin_memory()
+
+    def token_fn(plan):
+        T = plan.total_q
+        return qb[:T], kb[:T], vb[:T]
+
+    out = {}
+    for label, budget in (("chunked_512", 512), ("unchunked", long_prompt + n_dec)):
+        loop = ServeLoop(Hq, Hkv, D, pages, 1.0 / math.sqrt(D), max_num_batched_tokens=budget,
+                         max_pages_per_seq=mp, max_num_seqs=64)
+        for r in range(n_dec):
+            loop.add_request(r, ctx, new_tokens)
+        # bring every decode request past its prompt (untimed)
+        for _ in range(10 ** 4):
+            res = loop.step(token_fn)
+            loop.wait(res)
+            if (res.plan.q_lens == 1).sum() == n_dec:
+                break
+        times, tokens, arrivals = [], 0, 0
+        t_all = time.perf_counter()
+        for i in range(steps):
+            if i % every == 0:
+                loop.add_request(1000 + arrivals, long_prompt, 1)
+                arrivals += 1
+            t0 = time.perf_counter()
+            res = loop.step(token_fn)
+            loop.wait(res)
+            times.append(time.perf_counter() - t0)
+            tokens += res.plan.total_q
+        t_all = time.perf_counter() - t_all
+        ms = np.array(times) * 1e3
+        out[label] = {"budget": budget, "step_ms_p50": float(np.percentile(ms, 50)),
+                      "step_ms_p99": float(np.percentile(ms, 99)), "step_ms_max": float(ms.max()),
+                      "step_ms_mean": float(ms.mean()), "tokens_per_s": tokens / t_all,
+                      "prompts": arrivals}
+        loop.close()
+    c = out["chunked_512"]
+    return {"metric": "serving step time seen by decoding requests (p99)", "value": c["step_ms_p99"],
+            "unit": "ms", "n_gpus": 1, "higher_is_better": False, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16)",
+            "config": {"workload": f"{n_dec} requests decoding over {ctx}-token contexts; an "
+                                   f"{long_prompt}-token prompt arrives every {every} steps; "
+                                   f"{steps} timed steps; 32 q / 8 kv heads, head_dim 128",
+                       "step": "schedule + copy-in + append + attention + copy-out, waited"},
+            "chunked": out["chunked_512"], "unchunked": out["unchunked"]}
+
+
 def cpu_baseline(name, budget_s=15.0):
     s = OracleSample(name)
     rows = s.rows(4)
@@ -493,6 +563,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--serve", action="store_true",
+                    help="serving-loop step times with and without chunked prefill")
     ap.add_argument("--kv-swap", action="store_true",
                     help="time KV page swap-out / swap-in instead of the step")
     ap.add_argument("--rows", default="all", choices=["all", "logits"],
@@ -511,6 +583,10 @@ def main():
     if args.kv_swap:
         if rank == 0:
             print(json.dumps(run_kv_swap(args)), flush=True)
+        return
+    if args.serve:
+        if rank == 0:
+            print(json.dumps(run_serve(args)), flush=True)
         return
 
     if world > 1:
