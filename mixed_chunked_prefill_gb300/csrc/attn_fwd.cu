@@ -160,6 +160,7 @@ struct KParams {
   int32_t hq;
   int32_t G;
   int32_t dec_stages;  // decode ring stages (a multiple of the warps sharing one head)
+  int32_t spp_log2;    // log2 of 16-token blocks per cache page (page size 16, 32 or 64)
   float scale_log2;    // sm_scale * log2(e): scores live in log2 units
 };
 
@@ -167,14 +168,22 @@ struct Seg {
   int q_start, lq, lk, hist;
 };
 
-// Physical page of logical page `lp` of segment `seg`, or num_pages (an
-// out-of-range TMA coordinate: the copy fills zeros) with an error bit when
-// the block table names a page outside the pool.
-__device__ __forceinline__ int page_of(const KParams& p, int seg, int lp) {
-  const int v = p.bt[static_cast<size_t>(seg) * p.max_pages + lp];
-  if (v >= 0 && v < p.num_pages) return v;
+// The kernels move KV in 16-token blocks.  Block `lb` of segment `seg` lives in
+// cache page bt[seg][lb / (P/16)] at token (lb % (P/16)) * 16.  page_of packs
+// both as (page << spp_log2) | (lb % (P/16)); a block-table entry outside the
+// pool gives page num_pages (an out-of-range TMA coordinate: the copy fills
+// zeros) and an error bit.
+__device__ __forceinline__ int page_of(const KParams& p, int seg, int lb) {
+  const int v = p.bt[static_cast<size_t>(seg) * p.max_pages + (lb >> p.spp_log2)];
+  const int sub = lb & ((1 << p.spp_log2) - 1);
+  if (v >= 0 && v < p.num_pages) return (v << p.spp_log2) | sub;
   atomicOr(p.err, MCP_DEVERR_PAGE_RANGE);
-  return p.num_pages;
+  return p.num_pages << p.spp_log2;
+}
+// cache page and first token of a packed 16-token block
+__device__ __forceinline__ int blk_page(const KParams& p, int b) { return b >> p.spp_log2; }
+__device__ __forceinline__ int blk_tok(const KParams& p, int b) {
+  return (b & ((1 << p.spp_log2) - 1)) * kPageSize;
 }
 
 // ------------------------------------------------------------------------
@@ -280,9 +289,9 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       const int key0 = kv0 + tt * kKvTile;
       const int npg = (kv1 - key0 + kPageSize - 1) / kPageSize;  // pages of the tile inside the item
       const bool mine = lane < kPages / 2 && pg0 + lane < npg;
-      return mine ? page_of(p, it.seg, key0 / kPageSize + pg0 + lane) : p.num_pages;
+      return mine ? page_of(p, it.seg, key0 / kPageSize + pg0 + lane) : p.num_pages << p.spp_log2;
     };
-    int pg_next = ntiles > 0 ? fetch(0) : p.num_pages;
+    int pg_next = ntiles > 0 ? fetch(0) : p.num_pages << p.spp_log2;
     int t = 0;
     for (; t < ntiles; ++t) {
       const int s = t % NS;
@@ -302,13 +311,13 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
 #pragma unroll
             for (int h = 0; h < C::kHalves; ++h)
               ptx::tma_load_5d(dst + h * C::kHalfBytes + (pg0 + i) * kPageSize * 128, tm, bar, 0,
-                               h, it.kv_head, 0, pgs[i], pol);
+                               h, it.kv_head, blk_tok(p, pgs[i]), blk_page(p, pgs[i]), pol);
         } else {
           const uint32_t dst = sV(s);
 #pragma unroll
           for (int i = 0; i < kPages / 2; ++i)
-            ptx::tma_load_5d(dst + (pg0 + i) * C::kHeadBlock, tm, bar, 0, 0, 0, it.kv_head, pgs[i],
-                             pol);
+            ptx::tma_load_5d(dst + (pg0 + i) * C::kHeadBlock, tm, bar, 0, blk_tok(p, pgs[i]), 0,
+                             it.kv_head, blk_page(p, pgs[i]), pol);
         }
       }
       __syncwarp();
@@ -545,7 +554,8 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
     bool ok = true;
     for (int b0 = 0; ok && b0 < npg; b0 += 32) {
       const int n = npg - b0 < 32 ? npg - b0 : 32;
-      const int pg = lane < n ? page_of(p, it.seg, kv0 / kPageSize + b0 + lane) : p.num_pages;
+      const int pg = lane < n ? page_of(p, it.seg, kv0 / kPageSize + b0 + lane)
+                              : p.num_pages << p.spp_log2;
       for (int i = 0; i < n; ++i) {
         const int pi = b0 + i;
         const int s = pi % NS;
@@ -554,8 +564,9 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
         if (lane == 0) {
           const uint32_t dst = ring + s * stage_bytes;
           ptx::mbar_arrive_expect_tx(c.b(BFULL0 + s), stage_bytes);
-          ptx::tma_load_5d(dst, tm_kd, c.b(BFULL0 + s), 0, 0, 0, it.kv_head, pgi, pol);
-          ptx::tma_load_5d(dst + block, tm_vd, c.b(BFULL0 + s), 0, 0, 0, it.kv_head, pgi, pol);
+          const int tok = blk_tok(p, pgi), pgp = blk_page(p, pgi);
+          ptx::tma_load_5d(dst, tm_kd, c.b(BFULL0 + s), 0, tok, 0, it.kv_head, pgp, pol);
+          ptx::tma_load_5d(dst + block, tm_vd, c.b(BFULL0 + s), 0, tok, 0, it.kv_head, pgp, pol);
         }
         __syncwarp();
         issued = pi + 1;
@@ -949,7 +960,7 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
                           (cuuint64_t)a.page_size, (cuuint64_t)a.num_pages};
     cuuint64_t strides[4] = {128, (cuuint64_t)D * 2, (cuuint64_t)a.num_kv_heads * D * 2,
                              (cuuint64_t)a.page_size * a.num_kv_heads * D * 2};
-    cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)a.page_size, 1};
+    cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)kPageSize, 1};
     if (!encode(&tk, a.k_cache, 5, dims, strides, box, "k_cache")) return -1;
   }
   {
@@ -959,7 +970,7 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
                           (cuuint64_t)a.num_kv_heads, (cuuint64_t)a.num_pages};
     cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * D * 2, 128, (cuuint64_t)D * 2,
                              (cuuint64_t)a.page_size * a.num_kv_heads * D * 2};
-    cuuint32_t box[5] = {64, (cuuint32_t)a.page_size, (cuuint32_t)(D / 64), 1, 1};
+    cuuint32_t box[5] = {64, (cuuint32_t)kPageSize, (cuuint32_t)(D / 64), 1, 1};
     if (!encode(&tv, a.v_cache, 5, dims, strides, box, "v_cache")) return -1;
   }
   {
@@ -969,7 +980,7 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
                           (cuuint64_t)a.num_kv_heads, (cuuint64_t)a.num_pages};
     cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * D * 2, 128, (cuuint64_t)D * 2,
                              (cuuint64_t)a.page_size * a.num_kv_heads * D * 2};
-    cuuint32_t box[5] = {64, (cuuint32_t)a.page_size, (cuuint32_t)(D / 64), (cuuint32_t)HG, 1};
+    cuuint32_t box[5] = {64, (cuuint32_t)kPageSize, (cuuint32_t)(D / 64), (cuuint32_t)HG, 1};
     if (!encode(&tkd, a.k_cache, 5, dims, strides, box, "k_cache pages")) return -1;
     if (!encode(&tvd, a.v_cache, 5, dims, strides, box, "v_cache pages")) return -1;
   }
@@ -985,6 +996,7 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   kp.part_lse = a.part_lse;
   kp.err = a.error_word;
   kp.max_pages = a.max_pages_per_seq;
+  kp.spp_log2 = a.page_size == 64 ? 2 : (a.page_size == 32 ? 1 : 0);
   kp.num_pages = a.num_pages;
   kp.hq = a.num_q_heads;
   kp.G = G;

@@ -82,7 +82,9 @@ def test_valid_worked_layout_plans():
 @pytest.mark.parametrize("over,cu,sk,code", [
     (dict(num_q_heads=30), CU, SK, _capi.MCP_ERR_INVALID_ARG),          # H_q % H_kv
     (dict(head_dim=96), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
-    (dict(page_size=32), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
+    (dict(page_size=8), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
+    (dict(page_size=48), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
+    (dict(page_size=128), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
     (dict(num_pages=0), CU, SK, _capi.MCP_ERR_INVALID_ARG),
     (dict(max_pages_per_seq=100), CU, SK, _capi.MCP_ERR_INVALID_ARG),   # 10000 keys need 625 pages
     (dict(total_q=1811), CU, SK, _capi.MCP_ERR_INVALID_ARG),
@@ -342,3 +344,23 @@ def test_kv_copy_pages_validation_before_launch():
     assert lib.mcp_kv_copy_pages(ctypes.c_void_p(0x1008), p, 4, p, p, 4, 32, p, p, 1, None,
                                  None) == 1
     assert lib.mcp_kv_copy_pages(None, None, 0, None, None, 0, 32, None, None, 0, None, None) == 0
+
+
+@pytest.mark.parametrize("page_size", [32, 64])
+def test_larger_pages_plan_and_slot_mapping(page_size):
+    """Pages of 32 / 64 tokens: the plan is the same as with 16-token pages
+    (the kernels move 16-token blocks), the slot mapping follows the oracle."""
+    w16 = synth.make_workload("worked")
+    w = synth.make_workload_from_lengths("p", w16.num_q_heads, w16.num_kv_heads, w16.head_dim,
+                                         page_size, w16.sm_scale, w16.q_lens, w16.k_lens, 3)
+    cu, _, _, _ = oracle.segment_layout(w.q_lens, w.k_lens)
+    st, plan, items, comb = plan_host(desc_for(w), cu, w.k_lens)
+    assert st == 0
+    st16, plan16, items16, _ = plan_host(desc_for(w16), cu, w16.k_lens)
+    assert plan.num_items == plan16.num_items
+    assert np.array_equal(items, items16)
+    bt = w.block_tables()
+    table = oracle.page_table_from_block_tables(bt, w.k_lens, page_size)
+    want = oracle.new_token_slots(table, cu, w.k_lens)
+    got = mcp.build_slot_mapping(bt, cu, w.k_lens, page_size, w.num_pages)
+    assert np.array_equal(got, want)

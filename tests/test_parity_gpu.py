@@ -216,3 +216,24 @@ def test_full_size_sampled_rows(name):
     print(f"{name}: sampled rows {full_rows}: max|err| {err:.3g} relRMS {rr:.3g} lse {lerr:.3g}")
     assert err <= 2e-2 and rr <= 1e-2 and lerr <= 1e-2
     assert torch.isfinite(out).all()
+
+
+# ---------------------------------------------------------------------------
+# cache pages of 32 and 64 tokens (the kernels move 16-token blocks)
+# ---------------------------------------------------------------------------
+
+BIG_PAGE_CASES = {
+    "decode-edges": ([1] * 10, [1, 15, 16, 17, 31, 32, 33, 63, 64, 65]),
+    "mid-page": ([40, 77, 130], [45, 77 + 133, 130 + 250]),
+    "mixed": ([1, 1, 300, 2], [121, 46, 2000, 700]),
+}
+
+
+@pytest.mark.parametrize("page_size", [32, 64])
+@pytest.mark.parametrize("case", sorted(BIG_PAGE_CASES))
+def test_larger_pages(case, page_size):
+    q, k = BIG_PAGE_CASES[case]
+    w = synth.make_workload_from_lengths(f"{case}-p{page_size}", 32, 8, 128, page_size,
+                                         1 / math.sqrt(128), q, k, 4321)
+    full_parity(w, label=f"{case}/p{page_size}")
+    full_parity(w, options=opts(16, 128), label=f"{case}/p{page_size}/split")

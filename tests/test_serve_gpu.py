@@ -26,7 +26,7 @@ from harness import rel_rms
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-H_Q, H_KV, D, P = 8, 2, 128, 16
+H_Q, H_KV, D = 8, 2, 128
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -41,16 +41,16 @@ def library():
     return mcp.load()
 
 
-@pytest.mark.parametrize("swap", [False, True])
-def test_serving_loop_matches_oracle(swap):
+@pytest.mark.parametrize("swap,P", [(False, 16), (True, 16), (True, 32)])
+def test_serving_loop_matches_oracle(swap, P):
     from mixed_chunked_prefill_gb300.serve import ServeLoop
 
     rng = np.random.Generator(np.random.PCG64(77 + swap))
-    num_pages, mp = 40, 40
+    num_pages, mp = 40 * 16 // P, 40 * 16 // P
     scale = 1.0 / math.sqrt(D)
     loop = ServeLoop(H_Q, H_KV, D, num_pages, scale, max_num_batched_tokens=128,
                      max_pages_per_seq=mp, max_num_seqs=8, long_prefill_token_threshold=64,
-                     preempt_swap=swap, num_host_pages=80)
+                     preempt_swap=swap, num_host_pages=80, page_size=P)
     nreq = 8
     for r in range(nreq):
         loop.add_request(r, int(rng.integers(20, 300)), int(rng.integers(3, 20)),
