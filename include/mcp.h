@@ -539,6 +539,26 @@ mcp_status mcp_host_step_wait(mcp_host_step* step, int64_t ticket);
 /* Wait for every step in flight, then free the object (NULL is ignored). */
 mcp_status mcp_host_step_destroy(mcp_host_step* step);
 
+/* ------------------------------------------------------------------------- */
+/* Non-paged varlen forward                                                   */
+/* ------------------------------------------------------------------------- */
+/*
+ * [W] "Flash Attention 的 varlen 接口": the same right-aligned causal attention
+ * over packed, non-paged K and V -- k, v [total_k, H_kv, D] bf16 (device), the
+ * keys of segment s being rows cu_seqlens_k[s] .. cu_seqlens_k[s+1]-1
+ * (cu_seqlens_k [S+1] int32, device, non-decreasing, cu_seqlens_k[0] = 0,
+ * cu_seqlens_k[S] = total_k <= 2^30).  Plan with mcp_mixed_attn_plan (or
+ * _plan_rows) from HOST cu_seqlens_q and seqlens_k = diff(cu_seqlens_k), with
+ * page_size 16, max_pages_per_seq >= ceil(max seqlens_k / 16) and any
+ * num_pages >= 1 (no page pool is read).  q, out, lse, workspace as in
+ * mcp_mixed_attn_fwd; there is no append (the keys are given).
+ */
+mcp_status mcp_mixed_attn_fwd_varlen(const mcp_plan* plan, const void* q, const void* k,
+                                     const void* v, const int32_t* cu_seqlens_q,
+                                     const int32_t* cu_seqlens_k, int64_t total_k, void* out,
+                                     float* lse, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
 /* Device-check bits written to an error word. */
 #define MCP_DEVERR_TIMEOUT 0x1      /* a bounded mbarrier wait gave up           */
 #define MCP_DEVERR_PAGE_RANGE 0x2   /* a block-table page id outside the pool    */

@@ -29,6 +29,7 @@ __all__ = [
     "build_slot_mapping", "mixed_attn_plan", "mixed_attn_fwd", "check_device_errors",
     "workspace_error_word", "merge_states", "make_desc", "mixed_attn_fwd_noalloc",
     "mixed_attn_plan_rows", "build_logits_indices", "gather_rows", "kv_copy_pages",
+    "mixed_attn_varlen",
 ]
 
 
@@ -253,6 +254,45 @@ def mixed_attn_fwd(plan: Plan, q, k_cache, v_cache, block_tables, cu_seqlens_q, 
         _dev(workspace, torch.uint8, "workspace"),
         int(workspace.numel()) if workspace is not None else 0, _stream(stream))
     _capi.check(st, "mixed_attn_fwd")
+
+
+def mixed_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, sm_scale, out=None, lse=None,
+                      options: PlanOptions | None = None, stream=None):
+    """Right-aligned causal attention over packed non-paged K/V ([W] "Flash
+    Attention 的 varlen 接口"): q [T, H_q, D], k / v [total_k, H_kv, D] bf16
+    CUDA tensors; cu_seqlens_q / cu_seqlens_k host int arrays.  Plans, runs
+    and checks the device error word; returns ``out`` (and fills ``lse``)."""
+    import torch
+
+    lib = load()
+    cu_q = np.ascontiguousarray(np.asarray(cu_seqlens_q, dtype=np.int32))
+    cu_k = np.ascontiguousarray(np.asarray(cu_seqlens_k, dtype=np.int32))
+    S = int(cu_q.size) - 1
+    if cu_k.size != S + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k differ in length")
+    sk = np.diff(cu_k).astype(np.int32)
+    T, Hq, D = (int(x) for x in q.shape)
+    total_k, Hkv = int(k.shape[0]), int(k.shape[1])
+    if int(cu_k[-1]) != total_k or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k / v must be [cu_seqlens_k[-1], H_kv, D]")
+    mp = max(1, int((sk.max() + 15) // 16)) if S else 1
+    desc = make_desc(S, T, Hq, Hkv, D, 16, mp, 1, sm_scale)
+    sizing = mixed_attn_plan(desc, cu_q, sk, options)
+    ws = torch.empty(max(256, int(sizing.workspace_bytes)), dtype=torch.uint8, device=q.device)
+    plan = mixed_attn_plan(desc, cu_q, sk, options, ws, stream)
+    if out is None:
+        out = torch.empty_like(q)
+    cu_q_d = torch.from_numpy(cu_q).to(q.device)
+    cu_k_d = torch.from_numpy(cu_k).to(q.device)
+    st = lib.mcp_mixed_attn_fwd_varlen(
+        ctypes.byref(plan), _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"),
+        _dev(v, torch.bfloat16, "v"), _dev(cu_q_d, torch.int32, "cu_seqlens_q"),
+        _dev(cu_k_d, torch.int32, "cu_seqlens_k"), total_k, _dev(out, torch.bfloat16, "out"),
+        _dev(lse, torch.float32, "lse"), _dev(ws, torch.uint8, "workspace"), int(ws.numel()),
+        _stream(stream))
+    _capi.check(st, "mixed_attn_fwd_varlen")
+    check_device_errors(workspace_error_word(plan, ws), stream)
+    return out
 
 
 def workspace_error_word(plan: Plan, workspace) -> int:

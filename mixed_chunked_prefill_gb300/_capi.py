@@ -138,6 +138,9 @@ SIGNATURES = {
                                              POINTER(PlanOptions), c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p]),
+    "mcp_mixed_attn_fwd_varlen": (c_int32, [POINTER(Plan), c_void_p, c_void_p, c_void_p,
+                                            c_void_p, c_void_p, c_int64, c_void_p, c_void_p,
+                                            c_void_p, c_size_t, c_void_p]),
     "mcp_check_device_errors": (c_int32, [c_void_p, c_void_p]),
     "mcp_workspace_error_word": (c_void_p, [POINTER(Plan), c_void_p]),
     "mcp_merge_states": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,

@@ -161,6 +161,7 @@ struct KParams {
   int32_t G;
   int32_t dec_stages;  // decode ring stages (a multiple of the warps sharing one head)
   int32_t spp_log2;    // log2 of 16-token blocks per cache page (page size 16, 32 or 64)
+  const int32_t* cu_k; // non-paged K/V: first row of each segment's keys (else nullptr)
   float scale_log2;    // sm_scale * log2(e): scores live in log2 units
 };
 
@@ -174,6 +175,9 @@ struct Seg {
 // pool gives page num_pages (an out-of-range TMA coordinate: the copy fills
 // zeros) and an error bit.
 __device__ __forceinline__ int page_of(const KParams& p, int seg, int lb) {
+  // non-paged K/V: the block is rows cu_k[seg] + 16 lb ... of one tensor (the
+  // tensor maps then have a single "page" spanning every row)
+  if (p.cu_k) return p.cu_k[seg] + lb * kPageSize;
   const int v = p.bt[static_cast<size_t>(seg) * p.max_pages + (lb >> p.spp_log2)];
   const int sub = lb & ((1 << p.spp_log2) - 1);
   if (v >= 0 && v < p.num_pages) return (v << p.spp_log2) | sub;
@@ -181,9 +185,15 @@ __device__ __forceinline__ int page_of(const KParams& p, int seg, int lb) {
   return p.num_pages << p.spp_log2;
 }
 // cache page and first token of a packed 16-token block
-__device__ __forceinline__ int blk_page(const KParams& p, int b) { return b >> p.spp_log2; }
+__device__ __forceinline__ int blk_page(const KParams& p, int b) {
+  return p.cu_k ? 0 : b >> p.spp_log2;
+}
 __device__ __forceinline__ int blk_tok(const KParams& p, int b) {
-  return (b & ((1 << p.spp_log2) - 1)) * kPageSize;
+  return p.cu_k ? b : (b & ((1 << p.spp_log2) - 1)) * kPageSize;
+}
+// a block outside every tensor (TMA fills zeros)
+__device__ __forceinline__ int oob_block(const KParams& p) {
+  return p.cu_k ? (1 << 30) : p.num_pages << p.spp_log2;
 }
 
 // ------------------------------------------------------------------------
@@ -289,9 +299,9 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       const int key0 = kv0 + tt * kKvTile;
       const int npg = (kv1 - key0 + kPageSize - 1) / kPageSize;  // pages of the tile inside the item
       const bool mine = lane < kPages / 2 && pg0 + lane < npg;
-      return mine ? page_of(p, it.seg, key0 / kPageSize + pg0 + lane) : p.num_pages << p.spp_log2;
+      return mine ? page_of(p, it.seg, key0 / kPageSize + pg0 + lane) : oob_block(p);
     };
-    int pg_next = ntiles > 0 ? fetch(0) : p.num_pages << p.spp_log2;
+    int pg_next = ntiles > 0 ? fetch(0) : oob_block(p);
     int t = 0;
     for (; t < ntiles; ++t) {
       const int s = t % NS;
@@ -555,7 +565,7 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
     for (int b0 = 0; ok && b0 < npg; b0 += 32) {
       const int n = npg - b0 < 32 ? npg - b0 : 32;
       const int pg = lane < n ? page_of(p, it.seg, kv0 / kPageSize + b0 + lane)
-                              : p.num_pages << p.spp_log2;
+                              : oob_block(p);
       for (int i = 0; i < n; ++i) {
         const int pi = b0 + i;
         const int s = pi % NS;
@@ -874,7 +884,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   Seg sg;
   sg.q_start = p.cu_q[it.seg];
   sg.lq = p.cu_q[it.seg + 1] - sg.q_start;
-  sg.lk = p.seqlens_k[it.seg];
+  sg.lk = p.cu_k ? p.cu_k[it.seg + 1] - p.cu_k[it.seg] : p.seqlens_k[it.seg];
   sg.hist = sg.lk - sg.lq;
 
   if (prefill) {
@@ -954,32 +964,37 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
     cuuint32_t box[4] = {64, 1, (cuuint32_t)G, (cuuint32_t)TQ};
     if (!encode(&tq, a.q, 4, dims, strides, box, "q")) return -1;
   }
+  // Paged caches: [num_pages, P, H_kv, D].  Non-paged K/V: [total_k, H_kv, D],
+  // described as one page of total_k tokens (a block is then addressed by its
+  // first row as the token coordinate).
+  const bool contig = a.cu_seqlens_k != nullptr;
+  const cuuint64_t ntok = contig ? static_cast<cuuint64_t>(a.total_k > 0 ? a.total_k : 1)
+                                 : static_cast<cuuint64_t>(a.page_size);
+  const cuuint64_t npages = contig ? 1 : static_cast<cuuint64_t>(a.num_pages);
+  const cuuint64_t page_stride = ntok * a.num_kv_heads * D * 2;
   {
-    // one 64-column panel of one kv head of one page: dims {d, panel, head, token, page}
-    cuuint64_t dims[5] = {64, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads,
-                          (cuuint64_t)a.page_size, (cuuint64_t)a.num_pages};
+    // one 64-column panel of one kv head of 16 tokens: dims {d, panel, head, token, page}
+    cuuint64_t dims[5] = {64, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads, ntok, npages};
     cuuint64_t strides[4] = {128, (cuuint64_t)D * 2, (cuuint64_t)a.num_kv_heads * D * 2,
-                             (cuuint64_t)a.page_size * a.num_kv_heads * D * 2};
+                             page_stride};
     cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)kPageSize, 1};
     if (!encode(&tk, a.k_cache, 5, dims, strides, box, "k_cache")) return -1;
   }
   {
-    // a whole page of one kv head: dims {d, token, panel, head, page}, so that
+    // 16 tokens of one kv head: dims {d, token, panel, head, page}, so that
     // shared memory receives [panel][token][64]
-    cuuint64_t dims[5] = {64, (cuuint64_t)a.page_size, (cuuint64_t)(D / 64),
-                          (cuuint64_t)a.num_kv_heads, (cuuint64_t)a.num_pages};
+    cuuint64_t dims[5] = {64, ntok, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads, npages};
     cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * D * 2, 128, (cuuint64_t)D * 2,
-                             (cuuint64_t)a.page_size * a.num_kv_heads * D * 2};
+                             page_stride};
     cuuint32_t box[5] = {64, (cuuint32_t)kPageSize, (cuuint32_t)(D / 64), 1, 1};
     if (!encode(&tv, a.v_cache, 5, dims, strides, box, "v_cache")) return -1;
   }
   {
-    // a whole page for HG kv heads, dims ordered {d, token, panel, head, page}
+    // 16 tokens of HG kv heads, dims ordered {d, token, panel, head, page}
     // so that shared memory receives [head][panel][token][64]
-    cuuint64_t dims[5] = {64, (cuuint64_t)a.page_size, (cuuint64_t)(D / 64),
-                          (cuuint64_t)a.num_kv_heads, (cuuint64_t)a.num_pages};
+    cuuint64_t dims[5] = {64, ntok, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads, npages};
     cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * D * 2, 128, (cuuint64_t)D * 2,
-                             (cuuint64_t)a.page_size * a.num_kv_heads * D * 2};
+                             page_stride};
     cuuint32_t box[5] = {64, (cuuint32_t)kPageSize, (cuuint32_t)(D / 64), (cuuint32_t)HG, 1};
     if (!encode(&tkd, a.k_cache, 5, dims, strides, box, "k_cache pages")) return -1;
     if (!encode(&tvd, a.v_cache, 5, dims, strides, box, "v_cache pages")) return -1;
@@ -997,6 +1012,7 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   kp.err = a.error_word;
   kp.max_pages = a.max_pages_per_seq;
   kp.spp_log2 = a.page_size == 64 ? 2 : (a.page_size == 32 ? 1 : 0);
+  kp.cu_k = a.cu_seqlens_k;
   kp.num_pages = a.num_pages;
   kp.hq = a.num_q_heads;
   kp.G = G;

@@ -732,6 +732,62 @@ mcp_status mcp_mixed_attn_fwd(const mcp_plan* plan, const void* q, const void* k
   return okay();
 }
 
+mcp_status mcp_mixed_attn_fwd_varlen(const mcp_plan* plan, const void* q, const void* k,
+                                     const void* v, const int32_t* cu_seqlens_q,
+                                     const int32_t* cu_seqlens_k, int64_t total_k, void* out,
+                                     float* lse, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  if (!plan || plan->magic != kPlanMagic) return fail(MCP_ERR_INVALID_ARG, "plan not initialised");
+  const mcp_attn_desc& d = plan->desc;
+  if (d.page_size != mcp::kPageSize)
+    return fail(MCP_ERR_INVALID_ARG, "plan a non-paged step with page_size 16");
+  if (total_k < 0 || total_k > (int64_t(1) << 30))
+    return fail(MCP_ERR_INVALID_ARG, "total_k %lld outside [0, 2^30]", static_cast<long long>(total_k));
+  if (plan->num_items == 0) return okay();
+  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out || !workspace)
+    return fail(MCP_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return fail(MCP_ERR_INVALID_ARG, "q / k / v / out must be 16-byte aligned");
+  if (!aligned(workspace, 256)) return fail(MCP_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(MCP_ERR_INVALID_ARG, "lse not 4-byte aligned");
+  if (static_cast<int64_t>(workspace_bytes) < plan->workspace_bytes)
+    return fail(MCP_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %lld needed", workspace_bytes,
+                static_cast<long long>(plan->workspace_bytes));
+  char* ws = static_cast<char*>(workspace);
+  mcp::FwdArgs a;
+  a.q = q;
+  a.k_cache = k;
+  a.v_cache = v;
+  a.block_tables = nullptr;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.seqlens_k = nullptr;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.total_k = total_k;
+  a.out = out;
+  a.lse = lse;
+  a.items = reinterpret_cast<const mcp::WorkItem*>(ws + plan->off_items);
+  a.combine = reinterpret_cast<const mcp::CombineEntry*>(ws + plan->off_combine);
+  a.part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
+  a.part_lse = reinterpret_cast<float*>(ws + plan->off_part_lse);
+  a.error_word = reinterpret_cast<int32_t*>(ws + plan->off_error);
+  a.num_items = plan->num_items;
+  a.num_combine = plan->num_combine;
+  a.combine_rows = plan->combine_rows;
+  a.total_q = d.total_q;
+  a.num_q_heads = d.num_q_heads;
+  a.num_kv_heads = d.num_kv_heads;
+  a.head_dim = d.head_dim;
+  a.page_size = d.page_size;
+  a.max_pages_per_seq = d.max_pages_per_seq;
+  a.num_pages = d.num_pages;
+  a.sm_scale = d.sm_scale;
+  int e = mcp::launch_mixed_attn(a, stream);
+  if (e != 0) return cuda_fail(e, "mixed_attn_fwd launch");
+  e = mcp::launch_combine(a, stream);
+  if (e != 0) return cuda_fail(e, "combine launch");
+  return okay();
+}
+
 mcp_status mcp_check_device_errors(int32_t* error_word, void* stream) {
   if (!error_word) return fail(MCP_ERR_INVALID_ARG, "error_word is NULL");
   cudaStream_t cs = static_cast<cudaStream_t>(stream);

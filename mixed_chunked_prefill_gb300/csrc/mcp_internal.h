@@ -78,6 +78,10 @@ struct FwdArgs {
   int32_t max_pages_per_seq;
   int32_t num_pages;
   float sm_scale;
+  // non-paged K/V [total_k, H_kv, D] (cu_seqlens_k != nullptr): segment s's
+  // keys are rows cu_seqlens_k[s] .. cu_seqlens_k[s+1]-1; block tables unused
+  const int32_t* cu_seqlens_k = nullptr;
+  int64_t total_k = 0;
 };
 
 // Launchers (return a cudaError_t value; 0 = success).  Defined in *.cu.

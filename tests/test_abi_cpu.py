@@ -364,3 +364,29 @@ def test_larger_pages_plan_and_slot_mapping(page_size):
     want = oracle.new_token_slots(table, cu, w.k_lens)
     got = mcp.build_slot_mapping(bt, cu, w.k_lens, page_size, w.num_pages)
     assert np.array_equal(got, want)
+
+
+def test_varlen_fwd_validation_before_launch():
+    lib = mcp.load()
+    d = base_desc()
+    cu = np.array([0, 1, 2, 1810], dtype=np.int32)
+    sk = np.array([121, 46, 10000], dtype=np.int32)
+    plan = mcp.Plan()
+    opts = mcp.PlanOptions(152, 0, 0)  # no device query on the CPU
+    assert lib.mcp_mixed_attn_plan(ctypes.byref(d), cu.ctypes.data_as(ctypes.c_void_p),
+                                   sk.ctypes.data_as(ctypes.c_void_p), ctypes.byref(opts),
+                                   ctypes.byref(plan), None, 0, None) == 0
+    p = ctypes.c_void_p(0x1000)
+    assert lib.mcp_mixed_attn_fwd_varlen(None, p, p, p, p, p, 10, p, None, p, 1 << 30, None) == 1
+    assert lib.mcp_mixed_attn_fwd_varlen(ctypes.byref(plan), None, p, p, p, p, 10, p, None, p,
+                                         1 << 30, None) == 1
+    assert lib.mcp_mixed_attn_fwd_varlen(ctypes.byref(plan), p, p, p, p, p, -1, p, None, p,
+                                         1 << 30, None) == 1
+    # a plan for 32-token pages cannot drive the non-paged forward
+    d32 = base_desc(page_size=32, max_pages_per_seq=313)
+    plan32 = mcp.Plan()
+    assert lib.mcp_mixed_attn_plan(ctypes.byref(d32), cu.ctypes.data_as(ctypes.c_void_p),
+                                   sk.ctypes.data_as(ctypes.c_void_p), ctypes.byref(opts),
+                                   ctypes.byref(plan32), None, 0, None) == 0
+    assert lib.mcp_mixed_attn_fwd_varlen(ctypes.byref(plan32), p, p, p, p, p, 10, p, None, p,
+                                         1 << 30, None) == 1
