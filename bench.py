@@ -77,6 +77,25 @@ def algorithmic(w, rows=None):
                 fwd_bytes=kv_bytes + q_bytes + o_bytes, flops_tc=flops_tc, flops_dec=flops_dec)
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value of ``x`` over the ranks (the job is as slow as its
+    slowest replica); ``device``: where the collective's tensor lives (the
+    GPU under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput of ``world`` replicas that each processed
+    ``units_per_rank`` units, timed by the slowest one."""
+    return world * units_per_rank / seconds
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -240,13 +259,9 @@ def run_gpu(args, rank, world, local_rank):
     step.check()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     fwd_ms = [a.elapsed_time(b) for a, b in fwd_evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    tokens_per_s = world * w.total_q * args.steps / (total_ms / 1e3)
+    tokens_per_s = job_rate(w.total_q * args.steps, world, total_ms / 1e3)
 
     # end to end through the C ABI from pinned host buffers
     e2e = None
@@ -269,13 +284,9 @@ def run_gpu(args, rank, world, local_rank):
         for i in range(args.e2e_steps):
             ticket = hs.run(q_h, k_h, v_h, cu, w.k_lens, bt, k_cache, v_cache, outs_h[i & 1])
         hs.wait(ticket)  # the last step's output is in host memory (and every earlier one)
-        e2e_s = time.perf_counter() - t0
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
         hs.close()
-        if world > 1:
-            tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e2e_s = float(tt.item())
-        e2e = {"value": world * w.total_q * args.e2e_steps / e2e_s, "unit": UNIT,
+        e2e = {"value": job_rate(w.total_q * args.e2e_steps, world, e2e_s), "unit": UNIT,
                "h2d_bytes_per_step": int(hs.h2d_bytes), "d2h_bytes_per_step": int(hs.d2h_bytes),
                "ms_per_step": 1e3 * e2e_s / args.e2e_steps, "steps": args.e2e_steps}
 
