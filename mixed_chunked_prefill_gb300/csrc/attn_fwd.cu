@@ -36,6 +36,8 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <type_traits>
+
 #include "mcp.h"
 #include "mcp_internal.h"
 #include "ptx.cuh"
@@ -160,7 +162,8 @@ struct KParams {
   int32_t hq;
   int32_t G;
   int32_t dec_stages;  // decode ring stages (a multiple of the warps sharing one head)
-  int32_t spp_log2;    // log2 of 16-token blocks per cache page (page size 16, 32 or 64)
+  int32_t spp_log2;    // log2 of TMA boxes per cache page (0 for page size 8 and 16, 1: 32, 2: 64)
+  int32_t box_log2;    // log2 of tokens per TMA box: 3 for page size 8, else 4
   const int32_t* cu_k; // non-paged K/V: first row of each segment's keys (else nullptr)
   float scale_log2;    // sm_scale * log2(e): scores live in log2 units
 };
@@ -169,29 +172,30 @@ struct Seg {
   int q_start, lq, lk, hist;
 };
 
-// The kernels move KV in 16-token blocks.  Block `lb` of segment `seg` lives in
-// cache page bt[seg][lb / (P/16)] at token (lb % (P/16)) * 16.  page_of packs
-// both as (page << spp_log2) | (lb % (P/16)); a block-table entry outside the
-// pool gives page num_pages (an out-of-range TMA coordinate: the copy fills
-// zeros) and an error bit.
-__device__ __forceinline__ int page_of(const KParams& p, int seg, int lb) {
-  // non-paged K/V: the block is rows cu_k[seg] + 16 lb ... of one tensor (the
+// The kernels move KV in boxes of B = 16 tokens (page size 16, 32, 64) or
+// B = 8 tokens (page size 8).  Box `u` of segment `seg` lives in cache page
+// bt[seg][u / (P/B)] at token (u % (P/B)) * B.  box_of packs both as
+// (page << spp_log2) | (u % (P/B)); a block-table entry outside the pool gives
+// page num_pages (an out-of-range TMA coordinate: the copy fills zeros) and an
+// error bit.
+__device__ __forceinline__ int box_of(const KParams& p, int seg, int u) {
+  // non-paged K/V: the box is rows cu_k[seg] + B u ... of one tensor (the
   // tensor maps then have a single "page" spanning every row)
-  if (p.cu_k) return p.cu_k[seg] + lb * kPageSize;
-  const int v = p.bt[static_cast<size_t>(seg) * p.max_pages + (lb >> p.spp_log2)];
-  const int sub = lb & ((1 << p.spp_log2) - 1);
+  if (p.cu_k) return p.cu_k[seg] + (u << p.box_log2);
+  const int v = p.bt[static_cast<size_t>(seg) * p.max_pages + (u >> p.spp_log2)];
+  const int sub = u & ((1 << p.spp_log2) - 1);
   if (v >= 0 && v < p.num_pages) return (v << p.spp_log2) | sub;
   atomicOr(p.err, MCP_DEVERR_PAGE_RANGE);
   return p.num_pages << p.spp_log2;
 }
-// cache page and first token of a packed 16-token block
+// cache page and first token of a packed box
 __device__ __forceinline__ int blk_page(const KParams& p, int b) {
   return p.cu_k ? 0 : b >> p.spp_log2;
 }
 __device__ __forceinline__ int blk_tok(const KParams& p, int b) {
-  return p.cu_k ? b : (b & ((1 << p.spp_log2) - 1)) * kPageSize;
+  return p.cu_k ? b : (b & ((1 << p.spp_log2) - 1)) << p.box_log2;
 }
-// a block outside every tensor (TMA fills zeros)
+// a box outside every tensor (TMA fills zeros)
 __device__ __forceinline__ int oob_block(const KParams& p) {
   return p.cu_k ? (1 << 30) : p.num_pages << p.spp_log2;
 }
@@ -213,7 +217,6 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
   const uint32_t sQ = base + C::kOffQ;
   auto sK = [&](int s) { return base + C::kOffK + static_cast<uint32_t>(s * C::kKvBytes); };
   auto sV = [&](int s) { return base + C::kOffV + static_cast<uint32_t>(s * C::kKvBytes); };
-  constexpr int kPages = kKvTile / kPageSize;  // 8 pages per tile
 
   // Two warps issue the MMAs: warp 1 Q K^T, warp 0 P V.  Each waits only for
   // its own operands, so one warp's barrier waits overlap the other's MMAs
@@ -235,7 +238,11 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     const uint32_t tO = tmem + 256;  // O: columns [256, 256 + D)
     // descriptor of stage 0 built once; an MMA adds a byte offset >> 4 to the
     // start-address field (shared addresses stay below 256 KB: no carry out)
-    const uint64_t dV0 = ptx::sdesc_sw128(sV(0), kPageSize * 128, 1024);
+    // V stage: boxes of B tokens, each [panel][B tokens][128 B]: 64-column
+    // panels B * 128 bytes apart, 8-key groups 1024 bytes apart inside a
+    // 16-token box and one box (D/64 KB) apart with 8-token boxes
+    const int B = 1 << p.box_log2;
+    const uint64_t dV0 = ptx::sdesc_sw128(sV(0), B * 128, B == 16 ? 1024 : C::kHalves * 1024);
     bool ok = true;
     for (int t = 0; ok && t < ntiles; ++t) {
       // P(t) barriers alternate with the tile parity, like the S buffers: the
@@ -245,18 +252,18 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       const int s = t % C::kVStages;
       if (!(ok = wait_on(c, c.b(BV0 + s), (t / C::kVStages) & 1))) break;
       const int nval = kv1 - (kv0 + t * kKvTile);
-      if (nval < kKvTile && (nval & (kPageSize - 1))) {
-        // Rows past the item's last key inside its last page may be unused
+      if (nval < kKvTile && (nval & (B - 1))) {
+        // Rows past the item's last key inside its last box may be unused
         // cache slots holding anything (NaN included); P is 0 there but
         // 0 * NaN would reach O, so those V rows are zeroed.
-        const int r0 = nval, nr = ((nval + kPageSize - 1) & ~(kPageSize - 1)) - nval;
+        const int r0 = nval, nr = ((nval + B - 1) & ~(B - 1)) - nval;
         const int per_half = nr * 8;
         uint8_t* gV = gb + (sV(s) - base);
         for (int i = lane; i < per_half * C::kHalves; i += 32) {
           const int h = i / per_half, rem = i - h * per_half;
           const int r = r0 + rem / 8, ch = rem & 7;
-          *reinterpret_cast<uint4*>(gV + (r / kPageSize) * C::kHeadBlock + h * kPageSize * 128 +
-                                    (r % kPageSize) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(gV + (r >> p.box_log2) * (C::kHalves * B * 128) + h * B * 128 +
+                                    (r & (B - 1)) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
@@ -281,57 +288,67 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     drain_wait(c.abort, c.err, c.b(BQ), 0);
   } else if (warp >= 6) {
     // -------------------------------------- K/V producers: four warps
-    // warp 6: K pages 0-3, warp 7: K pages 4-7, warp 8: V pages 0-3, warp 9: V pages 4-7.
-    // A K tile arrives as one box per (page, 64-column panel) so that each
+    // warp 6: K boxes of keys 0-63, warp 7: K keys 64-127, warp 8: V keys 0-63,
+    // warp 9: V keys 64-127.  A box holds B = 16 (or 8) tokens of one page.
+    // A K tile arrives as one box per (box, 64-column panel) so that each
     // panel holds 128 consecutive keys (the K-major operand of Q K^T); a V tile
-    // arrives as one box per page, [panel][16 tokens][128 B], which P V reads
-    // one page (16 keys) per MMA.
+    // arrives as one box per box of tokens, [panel][B tokens][128 B], which
+    // P V reads 16 keys per MMA.
     const int pr = warp - 6;
     const bool isK = pr < 2;
-    const int pg0 = (pr & 1) * (kPages / 2);
     const CUtensorMap* tm = isK ? tm_k : tm_v;
     const uint64_t pol = ptx::policy_evict_last();  // other q tiles re-read these K/V
     const int NS = C::kKStages;
     const int full0 = isK ? BK0 : BV0, empty0 = isK ? BKE0 : BE0;
-    // the block-table entries of tile t + 1 are read while tile t is issued, so
-    // that the dependent global load is off the stage-refill path
-    auto fetch = [&](int tt) -> int {
-      const int key0 = kv0 + tt * kKvTile;
-      const int npg = (kv1 - key0 + kPageSize - 1) / kPageSize;  // pages of the tile inside the item
-      const bool mine = lane < kPages / 2 && pg0 + lane < npg;
-      return mine ? page_of(p, it.seg, key0 / kPageSize + pg0 + lane) : oob_block(p);
-    };
-    int pg_next = ntiles > 0 ? fetch(0) : oob_block(p);
-    int t = 0;
-    for (; t < ntiles; ++t) {
-      const int s = t % NS;
-      const int pg = pg_next;
-      if (t + 1 < ntiles) pg_next = fetch(t + 1);
-      if (t >= NS && !wait_on(c, c.b(empty0 + s), ((t / NS) + 1) & 1)) break;
-      int pgs[kPages / 2];
+    // the tile loop for boxes of B tokens; returns the tiles issued
+    auto produce = [&](auto box_tok) -> int {
+      constexpr int B = decltype(box_tok)::value;
+      constexpr int kLog = B == 16 ? 4 : 3;
+      constexpr int nu = (kKvTile / 2) / B;  // boxes of a tile this warp loads: 4 or 8
+      const int u0 = (pr & 1) * nu;
+      // the block-table entries of tile t + 1 are read while tile t is issued,
+      // so that the dependent global load is off the stage-refill path
+      auto fetch = [&](int tt) -> int {
+        const int key0 = kv0 + tt * kKvTile;
+        const int nbox = (kv1 - key0 + B - 1) >> kLog;  // boxes of the tile inside the item
+        const bool mine = lane < nu && u0 + lane < nbox;
+        return mine ? box_of(p, it.seg, (key0 >> kLog) + u0 + lane) : oob_block(p);
+      };
+      int pg_next = ntiles > 0 ? fetch(0) : oob_block(p);
+      int t = 0;
+      for (; t < ntiles; ++t) {
+        const int s = t % NS;
+        const int pg = pg_next;
+        if (t + 1 < ntiles) pg_next = fetch(t + 1);
+        if (t >= NS && !wait_on(c, c.b(empty0 + s), ((t / NS) + 1) & 1)) break;
+        int pgs[nu];
 #pragma unroll
-      for (int i = 0; i < kPages / 2; ++i) pgs[i] = __shfl_sync(0xffffffffu, pg, i);
-      if (lane == 0) {
-        const uint32_t bar = c.b(full0 + s);
-        ptx::mbar_arrive_expect_tx(bar, C::kKvBytes / 2);
-        if (isK) {
-          const uint32_t dst = sK(s);
+        for (int i = 0; i < nu; ++i) pgs[i] = __shfl_sync(0xffffffffu, pg, i);
+        if (lane == 0) {
+          const uint32_t bar = c.b(full0 + s);
+          ptx::mbar_arrive_expect_tx(bar, C::kKvBytes / 2);
+          if (isK) {
+            const uint32_t dst = sK(s);
 #pragma unroll
-          for (int i = 0; i < kPages / 2; ++i)
+            for (int i = 0; i < nu; ++i)
 #pragma unroll
-            for (int h = 0; h < C::kHalves; ++h)
-              ptx::tma_load_5d(dst + h * C::kHalfBytes + (pg0 + i) * kPageSize * 128, tm, bar, 0,
-                               h, it.kv_head, blk_tok(p, pgs[i]), blk_page(p, pgs[i]), pol);
-        } else {
-          const uint32_t dst = sV(s);
+              for (int h = 0; h < C::kHalves; ++h)
+                ptx::tma_load_5d(dst + h * C::kHalfBytes + (u0 + i) * B * 128, tm, bar, 0, h,
+                                 it.kv_head, blk_tok(p, pgs[i]), blk_page(p, pgs[i]), pol);
+          } else {
+            const uint32_t dst = sV(s);
 #pragma unroll
-          for (int i = 0; i < kPages / 2; ++i)
-            ptx::tma_load_5d(dst + (pg0 + i) * C::kHeadBlock, tm, bar, 0, blk_tok(p, pgs[i]), 0,
-                             it.kv_head, blk_page(p, pgs[i]), pol);
+            for (int i = 0; i < nu; ++i)
+              ptx::tma_load_5d(dst + (u0 + i) * (C::kHalves * B * 128), tm, bar, 0,
+                               blk_tok(p, pgs[i]), 0, it.kv_head, blk_page(p, pgs[i]), pol);
+          }
         }
+        __syncwarp();
       }
-      __syncwarp();
-    }
+      return t;
+    };
+    const int t = p.box_log2 == 4 ? produce(std::integral_constant<int, 16>{})
+                                  : produce(std::integral_constant<int, 8>{});
     // drain: the last tile this warp issued into each stage
     for (int s = 0; s < NS && s < t; ++s) {
       const int last = s + ((t - 1 - s) / NS) * NS;
@@ -554,29 +571,43 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
   const int kv0 = it.kv_begin, kv1 = it.kv_end;
   const int npg = (kv1 - kv0 + kPageSize - 1) / kPageSize;
   const int NS = p.dec_stages;
-  const int block = HG * C::kHeadBlock;        // K (or V) bytes of one page for the group
+  const int block = HG * C::kHeadBlock;        // K (or V) bytes of 16 tokens for the group
   const int stage_bytes = 2 * block;
   const uint32_t ring = base;
+  // a stage holds 16 tokens: one box of 16 or two boxes of 8, each box laid
+  // out [head][panel][B tokens][128 B]
+  const int B = 1 << p.box_log2;
+  const int ups = kPageSize >> p.box_log2;    // boxes per stage: 1 or 2
+  const int box_bytes = block / ups;
 
   if (warp == 0) {
     const uint64_t pol = ptx::policy_evict_first();  // each page is read once
     int issued = 0;
     bool ok = true;
-    for (int b0 = 0; ok && b0 < npg; b0 += 32) {
-      const int n = npg - b0 < 32 ? npg - b0 : 32;
-      const int pg = lane < n ? page_of(p, it.seg, kv0 / kPageSize + b0 + lane)
-                              : oob_block(p);
+    const int nbox = (kv1 - kv0 + B - 1) >> p.box_log2;  // boxes inside the item
+    const int per_batch = 32 / ups;                      // stages whose box ids one fetch covers
+    for (int b0 = 0; ok && b0 < npg; b0 += per_batch) {
+      const int n = npg - b0 < per_batch ? npg - b0 : per_batch;
+      const int ub = b0 * ups + lane;                    // box (inside the item) of this lane
+      const int pg = lane < n * ups && ub < nbox ? box_of(p, it.seg, (kv0 >> p.box_log2) + ub)
+                                                  : oob_block(p);
       for (int i = 0; i < n; ++i) {
         const int pi = b0 + i;
         const int s = pi % NS;
         if (pi >= NS && !(ok = wait_on(c, c.b(BEMPTY0 + s), ((pi / NS) + 1) & 1))) break;
-        const int pgi = __shfl_sync(0xffffffffu, pg, i);
+        const int pga = __shfl_sync(0xffffffffu, pg, i * ups);
+        const int pgb = __shfl_sync(0xffffffffu, pg, i * ups + ups - 1);
         if (lane == 0) {
           const uint32_t dst = ring + s * stage_bytes;
           ptx::mbar_arrive_expect_tx(c.b(BFULL0 + s), stage_bytes);
-          const int tok = blk_tok(p, pgi), pgp = blk_page(p, pgi);
-          ptx::tma_load_5d(dst, tm_kd, c.b(BFULL0 + s), 0, tok, 0, it.kv_head, pgp, pol);
-          ptx::tma_load_5d(dst + block, tm_vd, c.b(BFULL0 + s), 0, tok, 0, it.kv_head, pgp, pol);
+          for (int j = 0; j < ups; ++j) {
+            const int pgi = j ? pgb : pga;
+            const int tok = blk_tok(p, pgi), pgp = blk_page(p, pgi);
+            ptx::tma_load_5d(dst + j * box_bytes, tm_kd, c.b(BFULL0 + s), 0, tok, 0, it.kv_head,
+                             pgp, pol);
+            ptx::tma_load_5d(dst + block + j * box_bytes, tm_vd, c.b(BFULL0 + s), 0, tok, 0,
+                             it.kv_head, pgp, pol);
+          }
         }
         __syncwarp();
         issued = pi + 1;
@@ -628,11 +659,19 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
   float mlo = neg_inf(), mhi = neg_inf(), llo = 0.f, lhi = 0.f;
   bool ok = true;
   const int mi = lane >> 3, rr = lane & 7;
-  const uint32_t head_off = static_cast<uint32_t>(hw * C::kHeadBlock);
+  // byte offset of stage row tk (0-15) of this warp's head inside a K or V
+  // half-stage, and the stride between 64-column panels
+  auto row_off = [&](int tk) -> uint32_t {
+    return static_cast<uint32_t>((tk >> p.box_log2) * box_bytes + hw * (C::kHalves * B * 128) +
+                                 (tk & (B - 1)) * 128);
+  };
+  const uint32_t offK = row_off((mi >> 1) * 8 + rr);  // ldmatrix rows of the K fragments
+  const uint32_t offV = row_off((mi & 1) * 8 + rr);   // and of the transposed V fragments
+  const uint32_t pstr = static_cast<uint32_t>(B * 128);
   for (int pi = po; pi < npg; pi += ps) {
     const int s = pi % NS;
     if (!(ok = wait_on(c, c.b(BFULL0 + s), (pi / NS) & 1))) break;
-    const uint32_t kb = ring + s * stage_bytes + head_off;
+    const uint32_t kb = ring + s * stage_bytes;
     const uint32_t vb = kb + block;
     // two independent accumulator chains (even / odd k-steps) halve the MMA latency chain
     float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -640,10 +679,10 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const int h = kk >> 2, c0 = (kk & 3) * 2;
-      const int tk = (mi >> 1) * 8 + rr;  // matrices: (tok 0-7, c0) (0-7, c0+1) (8-15, c0) (8-15, c0+1)
+      // matrices: (tok 0-7, c0) (0-7, c0+1) (8-15, c0) (8-15, c0+1)
       const int ch = c0 + (mi & 1);
       uint32_t b0, b1, b2, b3;
-      ptx::ldsm_x4(kb + h * kPageSize * 128 + tk * 128 + ((ch ^ (tk & 7)) << 4), b0, b1, b2, b3);
+      ptx::ldsm_x4(kb + offK + h * pstr + ((ch ^ rr) << 4), b0, b1, b2, b3);
       float(*acc)[4] = (kk & 1) ? sb : sa;
       ptx::mma16816(acc[0], qa[kk], b0, b1);
       ptx::mma16816(acc[1], qa[kk], b2, b3);
@@ -698,10 +737,10 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
 #pragma unroll
     for (int dd = 0; dd < D / 16; ++dd) {
       const int h = dd >> 2, c0 = (dd & 3) * 2;
-      const int tk = (mi & 1) * 8 + rr;  // matrices: (tok 0-7, c0) (8-15, c0) (0-7, c0+1) (8-15, c0+1)
+      // matrices: (tok 0-7, c0) (8-15, c0) (0-7, c0+1) (8-15, c0+1)
       const int ch = c0 + (mi >> 1);
       uint32_t v0, v1, v2, v3;
-      ptx::ldsm_x4_t(vb + h * kPageSize * 128 + tk * 128 + ((ch ^ (tk & 7)) << 4), v0, v1, v2, v3);
+      ptx::ldsm_x4_t(vb + offV + h * pstr + ((ch ^ rr) << 4), v0, v1, v2, v3);
       if (nvalid < kPageSize) {
         // keys past the item's end: unused slots may hold NaN; P is 0 there
         v0 = keep_pair(v0, tig * 2, nvalid);
@@ -972,12 +1011,14 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
                                  : static_cast<cuuint64_t>(a.page_size);
   const cuuint64_t npages = contig ? 1 : static_cast<cuuint64_t>(a.num_pages);
   const cuuint64_t page_stride = ntok * a.num_kv_heads * D * 2;
+  // tokens per TMA box: 8 for page size 8, else 16 (a larger page is several boxes)
+  const int box_tok = (!contig && a.page_size == 8) ? 8 : kPageSize;
   {
     // one 64-column panel of one kv head of 16 tokens: dims {d, panel, head, token, page}
     cuuint64_t dims[5] = {64, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads, ntok, npages};
     cuuint64_t strides[4] = {128, (cuuint64_t)D * 2, (cuuint64_t)a.num_kv_heads * D * 2,
                              page_stride};
-    cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)kPageSize, 1};
+    cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)box_tok, 1};
     if (!encode(&tk, a.k_cache, 5, dims, strides, box, "k_cache")) return -1;
   }
   {
@@ -986,7 +1027,7 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
     cuuint64_t dims[5] = {64, ntok, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads, npages};
     cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * D * 2, 128, (cuuint64_t)D * 2,
                              page_stride};
-    cuuint32_t box[5] = {64, (cuuint32_t)kPageSize, (cuuint32_t)(D / 64), 1, 1};
+    cuuint32_t box[5] = {64, (cuuint32_t)box_tok, (cuuint32_t)(D / 64), 1, 1};
     if (!encode(&tv, a.v_cache, 5, dims, strides, box, "v_cache")) return -1;
   }
   {
@@ -995,7 +1036,7 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
     cuuint64_t dims[5] = {64, ntok, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads, npages};
     cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * D * 2, 128, (cuuint64_t)D * 2,
                              page_stride};
-    cuuint32_t box[5] = {64, (cuuint32_t)kPageSize, (cuuint32_t)(D / 64), (cuuint32_t)HG, 1};
+    cuuint32_t box[5] = {64, (cuuint32_t)box_tok, (cuuint32_t)(D / 64), (cuuint32_t)HG, 1};
     if (!encode(&tkd, a.k_cache, 5, dims, strides, box, "k_cache pages")) return -1;
     if (!encode(&tvd, a.v_cache, 5, dims, strides, box, "v_cache pages")) return -1;
   }
@@ -1011,7 +1052,8 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   kp.part_lse = a.part_lse;
   kp.err = a.error_word;
   kp.max_pages = a.max_pages_per_seq;
-  kp.spp_log2 = a.page_size == 64 ? 2 : (a.page_size == 32 ? 1 : 0);
+  kp.spp_log2 = contig ? 0 : (a.page_size == 64 ? 2 : (a.page_size == 32 ? 1 : 0));
+  kp.box_log2 = box_tok == 8 ? 3 : 4;
   kp.cu_k = a.cu_seqlens_k;
   kp.num_pages = a.num_pages;
   kp.hq = a.num_q_heads;

@@ -67,8 +67,8 @@ mcp_status validate_desc(const mcp_attn_desc* d) {
                 d->num_q_heads, d->num_kv_heads);
   if (d->head_dim != 64 && d->head_dim != 128)
     return fail(MCP_ERR_UNSUPPORTED, "head_dim %d (built: 64, 128)", d->head_dim);
-  if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
-    return fail(MCP_ERR_UNSUPPORTED, "page_size %d (built: 16, 32, 64)", d->page_size);
+  if (d->page_size != 8 && d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
+    return fail(MCP_ERR_UNSUPPORTED, "page_size %d (built: 8, 16, 32, 64)", d->page_size);
   if (d->num_q_heads / d->num_kv_heads > mcp::kTileRows)
     return fail(MCP_ERR_UNSUPPORTED, "group size %d > 128", d->num_q_heads / d->num_kv_heads);
   if (d->num_kv_heads > 32767)

@@ -13,8 +13,9 @@ constexpr int kDecodeMaxRows = 16;   // query rows of one kv head on the decode 
 constexpr int kDecodeMaxHeads = 8;   // kv heads one decode item covers (one consumer warp each)
 constexpr int kTileRows = 128;       // query rows of a tensor-core tile (TMEM lanes)
 constexpr int kKvTile = 128;         // keys per tensor-core KV tile
-constexpr int kPageSize = 16;        // tokens per KV block the kernels move (cache pages
-                                     // hold 1, 2 or 4 such blocks: page size 16, 32, 64)
+constexpr int kPageSize = 16;        // tokens per KV block the kernels step over (a cache
+                                     // page holds 1, 2 or 4 such blocks at page size 16,
+                                     // 32, 64; at page size 8 a block spans two pages)
 constexpr int kFwdThreads = 320;     // 10 warps: TMA producer, MMA issuer, 8 compute / producer
 
 // kv heads covered by one decode item: the largest power of two <= 8 dividing H_kv

@@ -82,7 +82,7 @@ def test_valid_worked_layout_plans():
 @pytest.mark.parametrize("over,cu,sk,code", [
     (dict(num_q_heads=30), CU, SK, _capi.MCP_ERR_INVALID_ARG),          # H_q % H_kv
     (dict(head_dim=96), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
-    (dict(page_size=8), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
+    (dict(page_size=4), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
     (dict(page_size=48), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
     (dict(page_size=128), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
     (dict(num_pages=0), CU, SK, _capi.MCP_ERR_INVALID_ARG),
@@ -346,10 +346,10 @@ def test_kv_copy_pages_validation_before_launch():
     assert lib.mcp_kv_copy_pages(None, None, 0, None, None, 0, 32, None, None, 0, None, None) == 0
 
 
-@pytest.mark.parametrize("page_size", [32, 64])
-def test_larger_pages_plan_and_slot_mapping(page_size):
-    """Pages of 32 / 64 tokens: the plan is the same as with 16-token pages
-    (the kernels move 16-token blocks), the slot mapping follows the oracle."""
+@pytest.mark.parametrize("page_size", [8, 32, 64])
+def test_other_page_sizes_plan_and_slot_mapping(page_size):
+    """Pages of 8 / 32 / 64 tokens: the plan is the same as with 16-token pages
+    (the kernels step over 16-token blocks), the slot mapping follows the oracle."""
     w16 = synth.make_workload("worked")
     w = synth.make_workload_from_lengths("p", w16.num_q_heads, w16.num_kv_heads, w16.head_dim,
                                          page_size, w16.sm_scale, w16.q_lens, w16.k_lens, 3)

@@ -219,21 +219,32 @@ def test_full_size_sampled_rows(name):
 
 
 # ---------------------------------------------------------------------------
-# cache pages of 32 and 64 tokens (the kernels move 16-token blocks)
+# cache pages of 8, 32 and 64 tokens (the kernels step over 16-token blocks,
+# loaded as one 16-token box, or as two 8-token boxes from 8-token pages)
 # ---------------------------------------------------------------------------
 
 BIG_PAGE_CASES = {
-    "decode-edges": ([1] * 10, [1, 15, 16, 17, 31, 32, 33, 63, 64, 65]),
+    "decode-edges": ([1] * 13, [1, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65]),
     "mid-page": ([40, 77, 130], [45, 77 + 133, 130 + 250]),
     "mixed": ([1, 1, 300, 2], [121, 46, 2000, 700]),
 }
 
 
-@pytest.mark.parametrize("page_size", [32, 64])
+@pytest.mark.parametrize("page_size", [8, 32, 64])
 @pytest.mark.parametrize("case", sorted(BIG_PAGE_CASES))
-def test_larger_pages(case, page_size):
+def test_other_page_sizes(case, page_size):
     q, k = BIG_PAGE_CASES[case]
     w = synth.make_workload_from_lengths(f"{case}-p{page_size}", 32, 8, 128, page_size,
                                          1 / math.sqrt(128), q, k, 4321)
     full_parity(w, label=f"{case}/p{page_size}")
     full_parity(w, options=opts(16, 128), label=f"{case}/p{page_size}/split")
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (6, 2, 64), (16, 1, 128)])
+def test_page8_head_shapes(hq, hkv, d):
+    """8-token pages with D = 64 (one 64-column panel) and other head groups."""
+    q, k = BIG_PAGE_CASES["mixed"]
+    w = synth.make_workload_from_lengths(f"p8-{hq}-{hkv}-{d}", hq, hkv, d, 8, 1 / math.sqrt(d),
+                                         q, k, 99)
+    full_parity(w, label=f"p8/{hq}/{hkv}/{d}")
+    full_parity(w, options=opts(16, 128), label=f"p8/{hq}/{hkv}/{d}/split")

@@ -41,7 +41,7 @@ def library():
     return mcp.load()
 
 
-@pytest.mark.parametrize("swap,P", [(False, 16), (True, 16), (True, 32)])
+@pytest.mark.parametrize("swap,P", [(False, 16), (True, 16), (True, 32), (False, 8)])
 def test_serving_loop_matches_oracle(swap, P):
     from mixed_chunked_prefill_gb300.serve import ServeLoop
 
