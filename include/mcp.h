@@ -127,7 +127,7 @@ typedef struct mcp_attn_desc {
   int32_t total_q;           /* T = cu_seqlens_q[S]                              */
   int32_t num_q_heads;       /* H_q                                              */
   int32_t num_kv_heads;      /* H_kv; must divide H_q                            */
-  int32_t head_dim;          /* D: 64 or 128                                     */
+  int32_t head_dim;          /* D: 64, 96 or 128 (96 runs zero-padded to 128)   */
   int32_t page_size;         /* P: 8, 16, 32 or 64                              */
   int32_t max_pages_per_seq; /* row length of block_tables                       */
   int32_t num_pages;         /* pages in each cache tensor                       */

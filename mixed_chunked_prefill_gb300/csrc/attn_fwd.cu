@@ -164,6 +164,9 @@ struct KParams {
   int32_t dec_stages;  // decode ring stages (a multiple of the warps sharing one head)
   int32_t spp_log2;    // log2 of TMA boxes per cache page (0 for page size 8 and 16, 1: 32, 2: 64)
   int32_t box_log2;    // log2 of tokens per TMA box: 3 for page size 8, else 4
+  int32_t dr;          // head_dim of the tensors (row width of q, out, K/V, partials): the
+                       // kernel's D, or 96 run as D = 128 (TMA fills columns 96-127 with 0)
+  int32_t panel_boxes; // 1: V and decode boxes cover one 64-column panel each (dr < D)
   const int32_t* cu_k; // non-paged K/V: first row of each segment's keys (else nullptr)
   float scale_log2;    // sm_scale * log2(e): scores live in log2 units
 };
@@ -230,7 +233,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(c.b(BQ), C::kHalves * G * TQ * 128);
       for (int h = 0; h < C::kHalves; ++h)
-        ptx::tma_load_4d(sQ + h * C::kHalfBytes, tm_q, c.b(BQ), 0, h, it.kv_head * G,
+        ptx::tma_load_3d(sQ + h * C::kHalfBytes, tm_q, c.b(BQ), 64 * h, it.kv_head * G,
                          sg.q_start + it.q_begin, ptx::policy_evict_first());
     }
     __syncwarp();
@@ -333,14 +336,23 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
             for (int i = 0; i < nu; ++i)
 #pragma unroll
               for (int h = 0; h < C::kHalves; ++h)
-                ptx::tma_load_5d(dst + h * C::kHalfBytes + (u0 + i) * B * 128, tm, bar, 0, h,
+                ptx::tma_load_4d(dst + h * C::kHalfBytes + (u0 + i) * B * 128, tm, bar, 64 * h,
                                  it.kv_head, blk_tok(p, pgs[i]), blk_page(p, pgs[i]), pol);
           } else {
             const uint32_t dst = sV(s);
 #pragma unroll
-            for (int i = 0; i < nu; ++i)
-              ptx::tma_load_5d(dst + (u0 + i) * (C::kHalves * B * 128), tm, bar, 0,
-                               blk_tok(p, pgs[i]), 0, it.kv_head, blk_page(p, pgs[i]), pol);
+            for (int i = 0; i < nu; ++i) {
+              if (!p.panel_boxes) {
+                ptx::tma_load_5d(dst + (u0 + i) * (C::kHalves * B * 128), tm, bar, 0,
+                                 blk_tok(p, pgs[i]), 0, it.kv_head, blk_page(p, pgs[i]), pol);
+              } else {  // one box per 64-column panel, same [panel][B tokens][128 B] layout
+#pragma unroll
+                for (int h = 0; h < C::kHalves; ++h)
+                  ptx::tma_load_4d(dst + (u0 + i) * (C::kHalves * B * 128) + h * B * 128, tm, bar,
+                                   64 * h, blk_tok(p, pgs[i]), it.kv_head, blk_page(p, pgs[i]),
+                                   pol);
+              }
+            }
           }
         }
         __syncwarp();
@@ -519,9 +531,9 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       uint32_t o[32];
       ptx::tmem_ld32(tO + j * 32, o);
       ptx::tmem_wait_ld();
-      if (store) {
+      if (store && j * 32 < p.dr) {  // columns past the tensors' head_dim are not stored
         if (direct) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + j * 32);
+          uint4* dst = reinterpret_cast<uint4*>(p.out + orow * p.dr + j * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             dst[v] = make_uint4(
@@ -532,7 +544,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
           }
         } else {
           float4* dst = reinterpret_cast<float4*>(
-              p.part_o + static_cast<size_t>(it.part_row + row) * D + j * 32);
+              p.part_o + static_cast<size_t>(it.part_row + row) * p.dr + j * 32);
 #pragma unroll
           for (int v = 0; v < 8; ++v)
             dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
@@ -603,10 +615,20 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
           for (int j = 0; j < ups; ++j) {
             const int pgi = j ? pgb : pga;
             const int tok = blk_tok(p, pgi), pgp = blk_page(p, pgi);
-            ptx::tma_load_5d(dst + j * box_bytes, tm_kd, c.b(BFULL0 + s), 0, tok, 0, it.kv_head,
-                             pgp, pol);
-            ptx::tma_load_5d(dst + block + j * box_bytes, tm_vd, c.b(BFULL0 + s), 0, tok, 0,
-                             it.kv_head, pgp, pol);
+            if (!p.panel_boxes) {  // [head][panel][B tokens][128 B]
+              ptx::tma_load_5d(dst + j * box_bytes, tm_kd, c.b(BFULL0 + s), 0, tok, 0, it.kv_head,
+                               pgp, pol);
+              ptx::tma_load_5d(dst + block + j * box_bytes, tm_vd, c.b(BFULL0 + s), 0, tok, 0,
+                               it.kv_head, pgp, pol);
+            } else {  // one box per panel: [panel][head][B tokens][128 B]
+              for (int h = 0; h < C::kHalves; ++h) {
+                const int off = j * box_bytes + h * HG * B * 128;
+                ptx::tma_load_4d(dst + off, tm_kd, c.b(BFULL0 + s), 64 * h, tok, it.kv_head, pgp,
+                                 pol);
+                ptx::tma_load_4d(dst + block + off, tm_vd, c.b(BFULL0 + s), 64 * h, tok,
+                                 it.kv_head, pgp, pol);
+              }
+            }
           }
         }
         __syncwarp();
@@ -641,16 +663,17 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
   uint32_t qa[D / 16][4];
   {
     const uint32_t* qlo = reinterpret_cast<const uint32_t*>(
-        p.q + (static_cast<size_t>(sg.q_start + it.q_begin + gid / G) * p.hq + head * G + gid % G) * D);
+        p.q + (static_cast<size_t>(sg.q_start + it.q_begin + gid / G) * p.hq + head * G + gid % G) * p.dr);
     const uint32_t* qhi = reinterpret_cast<const uint32_t*>(
         p.q + (static_cast<size_t>(sg.q_start + it.q_begin + (gid + 8) / G) * p.hq + head * G +
-               (gid + 8) % G) * D);
+               (gid + 8) % G) * p.dr);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      qa[kk][0] = vlo ? qlo[kk * 8 + tig] : 0u;
-      qa[kk][1] = vhi ? qhi[kk * 8 + tig] : 0u;
-      qa[kk][2] = vlo ? qlo[kk * 8 + 4 + tig] : 0u;
-      qa[kk][3] = vhi ? qhi[kk * 8 + 4 + tig] : 0u;
+      const bool in = kk * 16 < p.dr;  // columns past the tensors' head_dim are 0
+      qa[kk][0] = vlo && in ? qlo[kk * 8 + tig] : 0u;
+      qa[kk][1] = vhi && in ? qhi[kk * 8 + tig] : 0u;
+      qa[kk][2] = vlo && in ? qlo[kk * 8 + 4 + tig] : 0u;
+      qa[kk][3] = vhi && in ? qhi[kk * 8 + 4 + tig] : 0u;
     }
   }
   float o[D / 8][4];
@@ -661,13 +684,13 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
   const int mi = lane >> 3, rr = lane & 7;
   // byte offset of stage row tk (0-15) of this warp's head inside a K or V
   // half-stage, and the stride between 64-column panels
+  const int hstr = p.panel_boxes ? B * 128 : C::kHalves * B * 128;  // between heads
+  const uint32_t pstr = static_cast<uint32_t>(p.panel_boxes ? HG * B * 128 : B * 128);  // panels
   auto row_off = [&](int tk) -> uint32_t {
-    return static_cast<uint32_t>((tk >> p.box_log2) * box_bytes + hw * (C::kHalves * B * 128) +
-                                 (tk & (B - 1)) * 128);
+    return static_cast<uint32_t>((tk >> p.box_log2) * box_bytes + hw * hstr + (tk & (B - 1)) * 128);
   };
   const uint32_t offK = row_off((mi >> 1) * 8 + rr);  // ldmatrix rows of the K fragments
   const uint32_t offV = row_off((mi & 1) * 8 + rr);   // and of the transposed V fragments
-  const uint32_t pstr = static_cast<uint32_t>(B * 128);
   for (int pi = po; pi < npg; pi += ps) {
     const int s = pi % NS;
     if (!(ok = wait_on(c, c.b(BFULL0 + s), (pi / NS) & 1))) break;
@@ -775,16 +798,18 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
       const float inv = half ? ihi : ilo;
       const size_t orow = static_cast<size_t>(sg.q_start + tok) * p.hq + head * G + g;
       if (direct) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + orow * D);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + orow * p.dr);
 #pragma unroll
         for (int nb = 0; nb < D / 8; ++nb)
-          dst[(nb * 8 + tig * 2) / 2] = ptx::pack_bf16x2(o[nb][2 * half] * inv, o[nb][2 * half + 1] * inv);
+          if (nb * 8 < p.dr)
+            dst[(nb * 8 + tig * 2) / 2] = ptx::pack_bf16x2(o[nb][2 * half] * inv, o[nb][2 * half + 1] * inv);
       } else {
-        float* dst = p.part_o + static_cast<size_t>(it.part_row + hw * it.part_head_stride + r) * D;
+        float* dst = p.part_o + static_cast<size_t>(it.part_row + hw * it.part_head_stride + r) * p.dr;
 #pragma unroll
         for (int nb = 0; nb < D / 8; ++nb)
-          *reinterpret_cast<float2*>(dst + nb * 8 + tig * 2) =
-              make_float2(o[nb][2 * half] * inv, o[nb][2 * half + 1] * inv);
+          if (nb * 8 < p.dr)
+            *reinterpret_cast<float2*>(dst + nb * 8 + tig * 2) =
+                make_float2(o[nb][2 * half] * inv, o[nb][2 * half + 1] * inv);
       }
       if (tig == 0) {
         const float m = half ? mhi : mlo;
@@ -841,7 +866,7 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
   const int tok = it.q_begin + r / G;
   const int g = r - (r / G) * G;
   const size_t orow = static_cast<size_t>(sg.q_start + tok) * p.hq + head * G + g;
-  for (int d = 0; d < D / 2; d += 4) {
+  for (int d = 0; d < D / 2 && d0 + d < p.dr; d += 4) {
     float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -854,9 +879,9 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
     }
     if (direct) {
       uint2 pk2 = make_uint2(ptx::pack_bf16x2(a[0] * inv, a[1] * inv), ptx::pack_bf16x2(a[2] * inv, a[3] * inv));
-      *reinterpret_cast<uint2*>(p.out + orow * D + d0 + d) = pk2;
+      *reinterpret_cast<uint2*>(p.out + orow * p.dr + d0 + d) = pk2;
     } else {
-      *reinterpret_cast<float4*>(p.part_o + static_cast<size_t>(it.part_row + hw * it.part_head_stride + r) * D + d0 + d) =
+      *reinterpret_cast<float4*>(p.part_o + static_cast<size_t>(it.part_row + hw * it.part_head_stride + r) * p.dr + d0 + d) =
           make_float4(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv);
     }
   }
@@ -996,49 +1021,61 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   const int TQ = kTileRows / G;
   const int HG = decode_head_group(a.num_kv_heads);
   alignas(64) CUtensorMap tq, tk, tv, tkd, tvd;
+  // dr: head_dim of the tensors.  dr = 96 runs this D = 128 kernel: every map
+  // below spans dr columns and a 64-column box at column 64 gets zeros past
+  // column 96 (out-of-range elements), so Q, K and V are zero-padded to 128.
+  const int dr = a.head_dim;
+  const cuuint64_t dr2 = static_cast<cuuint64_t>(dr) * 2;
   {
-    cuuint64_t dims[4] = {64, (cuuint64_t)(D / 64), (cuuint64_t)a.num_q_heads,
+    // Q [T, H_q, dr]: dims {d, head, token}; a box is one 64-column panel of
+    // the G heads of one kv head for TQ tokens (column 64 h for panel h)
+    cuuint64_t dims[3] = {(cuuint64_t)dr, (cuuint64_t)a.num_q_heads,
                           (cuuint64_t)(a.total_q > 0 ? a.total_q : 1)};
-    cuuint64_t strides[3] = {128, (cuuint64_t)D * 2, (cuuint64_t)a.num_q_heads * D * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)G, (cuuint32_t)TQ};
-    if (!encode(&tq, a.q, 4, dims, strides, box, "q")) return -1;
+    cuuint64_t strides[2] = {dr2, (cuuint64_t)a.num_q_heads * dr2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
+    if (!encode(&tq, a.q, 3, dims, strides, box, "q")) return -1;
   }
-  // Paged caches: [num_pages, P, H_kv, D].  Non-paged K/V: [total_k, H_kv, D],
+  // Paged caches: [num_pages, P, H_kv, dr].  Non-paged K/V: [total_k, H_kv, dr],
   // described as one page of total_k tokens (a block is then addressed by its
   // first row as the token coordinate).
   const bool contig = a.cu_seqlens_k != nullptr;
   const cuuint64_t ntok = contig ? static_cast<cuuint64_t>(a.total_k > 0 ? a.total_k : 1)
                                  : static_cast<cuuint64_t>(a.page_size);
   const cuuint64_t npages = contig ? 1 : static_cast<cuuint64_t>(a.num_pages);
-  const cuuint64_t page_stride = ntok * a.num_kv_heads * D * 2;
+  const cuuint64_t page_stride = ntok * a.num_kv_heads * dr2;
   // tokens per TMA box: 8 for page size 8, else 16 (a larger page is several boxes)
   const int box_tok = (!contig && a.page_size == 8) ? 8 : kPageSize;
+  const bool panel_boxes = dr != D;
   {
-    // one 64-column panel of one kv head of 16 tokens: dims {d, panel, head, token, page}
-    cuuint64_t dims[5] = {64, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads, ntok, npages};
-    cuuint64_t strides[4] = {128, (cuuint64_t)D * 2, (cuuint64_t)a.num_kv_heads * D * 2,
-                             page_stride};
-    cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)box_tok, 1};
-    if (!encode(&tk, a.k_cache, 5, dims, strides, box, "k_cache")) return -1;
+    // one 64-column panel of one kv head of box_tok tokens: dims {d, head, token, page}
+    cuuint64_t dims[4] = {(cuuint64_t)dr, (cuuint64_t)a.num_kv_heads, ntok, npages};
+    cuuint64_t strides[3] = {dr2, (cuuint64_t)a.num_kv_heads * dr2, page_stride};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_tok, 1};
+    if (!encode(&tk, a.k_cache, 4, dims, strides, box, "k_cache")) return -1;
   }
-  {
-    // 16 tokens of one kv head: dims {d, token, panel, head, page}, so that
-    // shared memory receives [panel][token][64]
+  if (!panel_boxes) {
+    // box_tok tokens of one kv head: dims {d, token, panel, head, page}, so
+    // that shared memory receives [panel][token][64] from one box
     cuuint64_t dims[5] = {64, ntok, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads, npages};
-    cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * D * 2, 128, (cuuint64_t)D * 2,
-                             page_stride};
+    cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * dr2, 128, dr2, page_stride};
     cuuint32_t box[5] = {64, (cuuint32_t)box_tok, (cuuint32_t)(D / 64), 1, 1};
     if (!encode(&tv, a.v_cache, 5, dims, strides, box, "v_cache")) return -1;
-  }
-  {
-    // 16 tokens of HG kv heads, dims ordered {d, token, panel, head, page}
+    // box_tok tokens of HG kv heads, dims ordered {d, token, panel, head, page}
     // so that shared memory receives [head][panel][token][64]
-    cuuint64_t dims[5] = {64, ntok, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads, npages};
-    cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * D * 2, 128, (cuuint64_t)D * 2,
-                             page_stride};
-    cuuint32_t box[5] = {64, (cuuint32_t)box_tok, (cuuint32_t)(D / 64), (cuuint32_t)HG, 1};
-    if (!encode(&tkd, a.k_cache, 5, dims, strides, box, "k_cache pages")) return -1;
-    if (!encode(&tvd, a.v_cache, 5, dims, strides, box, "v_cache pages")) return -1;
+    cuuint32_t boxd[5] = {64, (cuuint32_t)box_tok, (cuuint32_t)(D / 64), (cuuint32_t)HG, 1};
+    if (!encode(&tkd, a.k_cache, 5, dims, strides, boxd, "k_cache pages")) return -1;
+    if (!encode(&tvd, a.v_cache, 5, dims, strides, boxd, "v_cache pages")) return -1;
+  } else {
+    // a panel boundary inside the row: one box per 64-column panel, dims
+    // {d, token, head, page}; a box lands as [token][64] (V) or
+    // [head][token][64] (decode, HG heads)
+    cuuint64_t dims[4] = {(cuuint64_t)dr, ntok, (cuuint64_t)a.num_kv_heads, npages};
+    cuuint64_t strides[3] = {(cuuint64_t)a.num_kv_heads * dr2, dr2, page_stride};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_tok, 1, 1};
+    if (!encode(&tv, a.v_cache, 4, dims, strides, box, "v_cache")) return -1;
+    cuuint32_t boxd[4] = {64, (cuuint32_t)box_tok, (cuuint32_t)HG, 1};
+    if (!encode(&tkd, a.k_cache, 4, dims, strides, boxd, "k_cache pages")) return -1;
+    if (!encode(&tvd, a.v_cache, 4, dims, strides, boxd, "v_cache pages")) return -1;
   }
   KParams kp;
   kp.items = a.items;
@@ -1054,6 +1091,8 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   kp.max_pages = a.max_pages_per_seq;
   kp.spp_log2 = contig ? 0 : (a.page_size == 64 ? 2 : (a.page_size == 32 ? 1 : 0));
   kp.box_log2 = box_tok == 8 ? 3 : 4;
+  kp.dr = dr;
+  kp.panel_boxes = panel_boxes ? 1 : 0;
   kp.cu_k = a.cu_seqlens_k;
   kp.num_pages = a.num_pages;
   kp.hq = a.num_q_heads;
@@ -1075,7 +1114,7 @@ int launch_mixed_attn(const FwdArgs& a, void* stream) {
   g_detail[0] = 0;
   if (a.num_items <= 0) return 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (a.head_dim == 128) return launch_fwd_d<128>(a, st);
+  if (a.head_dim == 128 || a.head_dim == 96) return launch_fwd_d<128>(a, st);
   if (a.head_dim == 64) return launch_fwd_d<64>(a, st);
   snprintf(g_detail, sizeof(g_detail), "head_dim %d not built", a.head_dim);
   return -1;

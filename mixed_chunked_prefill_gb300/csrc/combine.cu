@@ -84,10 +84,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineEntry* __rest
         acc[1] += wj * o.y;
         acc[2] += wj * o.z;
         acc[3] += wj * o.w;
-      } else {
+      } else if constexpr (V == 2) {
         const float2 o = __ldg(reinterpret_cast<const float2*>(src));
         acc[0] += wj * o.x;
         acc[1] += wj * o.y;
+      } else {
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] += wj * __ldg(src + v);
       }
     }
   }
@@ -100,8 +103,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineEntry* __rest
     uint2* dst = reinterpret_cast<uint2*>(out + orow * D + lane * V);
     *dst = make_uint2(ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv),
                       ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv));
-  } else {
+  } else if constexpr (V == 2) {
     *reinterpret_cast<uint32_t*>(out + orow * D + lane * V) = ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  } else {
+#pragma unroll
+    for (int v = 0; v < V; ++v) out[orow * D + lane * V + v] = __float2bfloat16_rn(acc[v] * inv);
   }
   if (lse && lane == 0) lse[orow] = L > 0.f ? M + logf(L) : neg_inf();
 }
@@ -145,6 +151,10 @@ int launch_combine(const FwdArgs& a, void* stream) {
   const int blocks = (a.combine_rows + 7) / 8;
   if (a.head_dim == 128) {
     combine_kernel<128><<<blocks, 256, 0, st>>>(
+        a.combine, a.num_combine, a.combine_rows, a.cu_seqlens_q, a.part_o, a.part_lse,
+        static_cast<__nv_bfloat16*>(a.out), a.lse, a.num_q_heads, G);
+  } else if (a.head_dim == 96) {
+    combine_kernel<96><<<blocks, 256, 0, st>>>(
         a.combine, a.num_combine, a.combine_rows, a.cu_seqlens_q, a.part_o, a.part_lse,
         static_cast<__nv_bfloat16*>(a.out), a.lse, a.num_q_heads, G);
   } else {

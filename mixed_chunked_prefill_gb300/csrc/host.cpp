@@ -65,8 +65,8 @@ mcp_status validate_desc(const mcp_attn_desc* d) {
   if (d->num_q_heads % d->num_kv_heads != 0)
     return fail(MCP_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
                 d->num_q_heads, d->num_kv_heads);
-  if (d->head_dim != 64 && d->head_dim != 128)
-    return fail(MCP_ERR_UNSUPPORTED, "head_dim %d (built: 64, 128)", d->head_dim);
+  if (d->head_dim != 64 && d->head_dim != 96 && d->head_dim != 128)
+    return fail(MCP_ERR_UNSUPPORTED, "head_dim %d (built: 64, 96, 128)", d->head_dim);
   if (d->page_size != 8 && d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
     return fail(MCP_ERR_UNSUPPORTED, "page_size %d (built: 8, 16, 32, 64)", d->page_size);
   if (d->num_q_heads / d->num_kv_heads > mcp::kTileRows)

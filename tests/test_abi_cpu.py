@@ -81,7 +81,7 @@ def test_valid_worked_layout_plans():
 
 @pytest.mark.parametrize("over,cu,sk,code", [
     (dict(num_q_heads=30), CU, SK, _capi.MCP_ERR_INVALID_ARG),          # H_q % H_kv
-    (dict(head_dim=96), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
+    (dict(head_dim=80), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
     (dict(page_size=4), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
     (dict(page_size=48), CU, SK, _capi.MCP_ERR_UNSUPPORTED),
     (dict(page_size=128), CU, SK, _capi.MCP_ERR_UNSUPPORTED),

@@ -41,7 +41,7 @@ def test_arena_bytes_cover_two_slots():
 
 
 @pytest.mark.parametrize("sh,lim,code", [
-    (shape(d=96), limits(), 2),
+    (shape(d=80), limits(), 2),
     (shape(p=4), limits(), 2),
     (shape(hq=30, hkv=8), limits(), 1),
     (shape(scale=0.0), limits(), 1),

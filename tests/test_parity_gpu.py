@@ -123,7 +123,8 @@ EDGE = {
 
 
 @pytest.mark.parametrize("case", sorted(EDGE))
-@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (4, 4, 64), (16, 1, 128), (6, 2, 64)])
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (4, 4, 64), (16, 1, 128), (6, 2, 64),
+                                      (32, 8, 96), (12, 3, 96)])
 def test_edge_cases(case, hq, hkv, d):
     q, k = EDGE[case]
     w = synth.make_workload_from_lengths(case, hq, hkv, d, 16, 1 / math.sqrt(d), q, k, 1234)
@@ -240,9 +241,10 @@ def test_other_page_sizes(case, page_size):
     full_parity(w, options=opts(16, 128), label=f"{case}/p{page_size}/split")
 
 
-@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (6, 2, 64), (16, 1, 128)])
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (6, 2, 64), (16, 1, 128), (32, 8, 96)])
 def test_page8_head_shapes(hq, hkv, d):
-    """8-token pages with D = 64 (one 64-column panel) and other head groups."""
+    """8-token pages with D = 64 (one 64-column panel), D = 96 (one box per
+    panel) and other head groups."""
     q, k = BIG_PAGE_CASES["mixed"]
     w = synth.make_workload_from_lengths(f"p8-{hq}-{hkv}-{d}", hq, hkv, d, 8, 1 / math.sqrt(d),
                                          q, k, 99)
