@@ -8,20 +8,28 @@
 //
 //  * tensor-core item -- 128 query rows (the G query heads of one kv head
 //    packed with 128/G tokens) against a KV range in 128-key tiles.  Warp 0
-//    loads the Q tile with TMA; warps 6-9 load each K/V tile page by page
-//    through the block table (a tile is 8 pages x 2 panels x K,V = 32 TMA
-//    boxes, split over four warps because one warp issues boxes serially);
-//    warp 1 issues tcgen05.mma (S = Q K^T into TMEM, O += P V into TMEM);
-//    warps 2-5 run the online softmax on S rows read from TMEM, write P (bf16)
-//    to shared memory and rescale O lazily.  Only tiles that cross the
-//    diagonal are masked ([K] "掩码特化").
+//    loads the Q tile with TMA and then issues O += P V; warp 1 issues
+//    S = Q K^T (A = Q, copied once into TMEM by the softmax warps; B = the K
+//    tile in shared memory); warps 6-9 load each K/V tile box by box through
+//    the block table (8 boxes x D/64 panels of K plus 8 boxes of V for 16-token
+//    boxes, twice as many 8-token boxes for 8-token pages), split over four
+//    warps because one warp issues its boxes serially; warps 2-5 run the
+//    online softmax on S rows read from TMEM, write bf16 P over the scores
+//    they read (S buffer t & 1) and rescale O lazily.  Only tiles that cross
+//    the diagonal are masked ([K] "掩码特化").
 //  * decode item -- the G*Lq (<= 16) query rows of each kv head of a head group
-//    (up to 8 heads) against a KV range.  Warp 0 streams whole pages for the
-//    group -- one TMA box per K page and one per V page, laid out in shared
-//    memory as [head][panel][token][64] -- through a multi-stage ring; warps 2-9
-//    each own one kv head (ldmatrix + mma.sync m16n8k16, quad-shuffle max/sum,
-//    online softmax); several warps share a head when the group is smaller
-//    than 8 and merge their states at the end.
+//    (up to 8 heads) against a KV range.  Warp 0 streams 16 tokens of the
+//    group per ring stage -- one TMA box for K and one for V, laid out in
+//    shared memory as [head][panel][token][64] (two boxes each for 8-token
+//    pages) -- through a multi-stage ring; warps 2-9 each own one kv head
+//    (ldmatrix + mma.sync m16n8k16, quad-shuffle max/sum, online softmax);
+//    several warps share a head when the group is smaller than 8 and merge
+//    their states at the end.
+//
+// head_dim 96 runs the D = 128 instantiation on 96-wide tensors: the tensor
+// maps span 96 columns, TMA fills columns 96-127 of every box with zeros, V
+// and decode stages take one box per 64-column panel, and only 96 columns of
+// O are stored.
 //
 // A split KV range writes (O, LSE) partials that combine.cu merges.
 //
