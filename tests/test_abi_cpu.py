@@ -390,3 +390,18 @@ def test_varlen_fwd_validation_before_launch():
                                    ctypes.byref(plan32), None, 0, None) == 0
     assert lib.mcp_mixed_attn_fwd_varlen(ctypes.byref(plan32), p, p, p, p, p, 10, p, None, p,
                                          1 << 30, None) == 1
+
+
+def test_head_dim_96_plans_with_96_wide_partials():
+    """head_dim 96 runs the D = 128 kernel on 96-wide tensors: the plan is the
+    one for D = 128, and the split partials are 96 floats per row."""
+    d96 = base_desc(head_dim=96, sm_scale=1 / math.sqrt(96))
+    d128 = base_desc()
+    st96, p96, items96, _ = plan_host(d96, CU, SK, dsplit=16, psplit=128)
+    st128, p128, items128, _ = plan_host(d128, CU, SK, dsplit=16, psplit=128)
+    assert st96 == 0 and st128 == 0
+    assert p96.num_items == p128.num_items and np.array_equal(items96, items128)
+    rows = p96.partial_rows
+    assert rows > 0
+    assert p96.off_part_lse - p96.off_part_o >= rows * 96 * 4
+    assert p96.off_part_lse - p96.off_part_o < rows * 128 * 4
