@@ -235,8 +235,22 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
       else pre_ns += H * (item_ns + cdiv(vis_of(x), mcp::kKvTile) * tile_ns);
     }
     if (pre_ns > 0.0 && dec_ns < 0.1 * (pre_ns + dec_ns)) {
+      // items of a candidate split (same for every candidate that splits no
+      // unit differently); evaluating only distinct candidates and none past
+      // eight items per SM keeps the search to a few list schedules
+      auto signature = [&](int64_t cand_ps) {
+        uint64_t sig = 1469598103934665603ull;  // FNV-1a over the units' split counts
+        for (const Unit& x : units) {
+          if (x.decode) continue;
+          int64_t n, sz;
+          even_split(vis_of(x), cand_ps, mcp::kKvTile, &n, &sz);
+          sig = (sig ^ static_cast<uint64_t>(n)) * 1099511628211ull;
+        }
+        return static_cast<int64_t>(sig & 0x7fffffffffffffffull);
+      };
+      std::vector<double> cost, load;
       auto makespan = [&](int64_t cand_ps) {
-        std::vector<double> cost;
+        cost.clear();
         for (const Unit& x : units) {
           int64_t n, sz;
           if (x.decode) {
@@ -255,19 +269,24 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
           }
         }
         std::sort(cost.begin(), cost.end(), std::greater<double>());
-        std::vector<double> load(static_cast<size_t>(std::max(1, num_sms)), 0.0);
-        std::make_heap(load.begin(), load.end(), std::greater<double>());
-        for (double c : cost) {  // longest first onto the least-loaded SM
+        load.assign(static_cast<size_t>(std::max(1, num_sms)), 0.0);
+        for (double c : cost) {  // longest first onto the least-loaded SM (a min-heap)
           std::pop_heap(load.begin(), load.end(), std::greater<double>());
           load.back() += c;
           std::push_heap(load.begin(), load.end(), std::greater<double>());
         }
         return *std::max_element(load.begin(), load.end());
       };
-      int64_t best = ps;
-      double best_t = makespan(ps);
+      const double t0 = makespan(ps);
+      const int64_t ps_sig = signature(ps);
+      int64_t best = ps, last_sig = -1;
+      double best_t = t0;
       for (int64_t cand = 65536; cand >= 2048; cand /= 2) {
-        const double t = makespan(cand);
+        if (count(ds, cand) > 8LL * std::max(1, num_sms)) break;  // counts grow as cand shrinks
+        const int64_t sig = signature(cand);
+        if (sig == last_sig) continue;  // the previous, larger candidate had the same items
+        last_sig = sig;
+        const double t = sig == ps_sig ? t0 : makespan(cand);
         if (t < best_t * 0.98 || (t <= best_t * 1.02 && cand > best)) {
           if (t < best_t) best_t = t;
           best = cand;
