@@ -216,10 +216,19 @@ def run_gpu(args, rank, world, local_rank):
                       stream=stream)
         del t["k_hist"], t["v_hist"]
         cu = np.concatenate([[0], np.cumsum(w.q_lens)]).astype(np.int32)
-        t0 = time.perf_counter()
         step = MixedStep(w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size, w.num_pages,
                          w.sm_scale, cu, w.k_lens, bt, device=dev, stream=stream, rows=rows)
-        plan_us = (time.perf_counter() - t0) * 1e6
+        # host planning of one step (the work the host step repeats per step):
+        # median of 20 plans from host metadata, no upload
+        plan_times = []
+        for _ in range(20):
+            t0 = time.perf_counter()
+            if rows is None:
+                mcp.mixed_attn_plan(step.desc, cu, w.k_lens, step.options)
+            else:
+                mcp.mixed_attn_plan_rows(step.desc, cu, w.k_lens, rows, step.options)
+            plan_times.append((time.perf_counter() - t0) * 1e6)
+        plan_us = statistics.median(plan_times)
         q, k_new, v_new = t["q"], t["k_new"], t["v_new"]
         out = torch.empty_like(q)
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
