@@ -127,7 +127,7 @@ typedef struct mcp_attn_desc {
   int32_t total_q;           /* T = cu_seqlens_q[S]                              */
   int32_t num_q_heads;       /* H_q                                              */
   int32_t num_kv_heads;      /* H_kv; must divide H_q                            */
-  int32_t head_dim;          /* D: 64, 96 or 128 (96 runs zero-padded to 128)   */
+  int32_t head_dim;          /* D: 64, 96, 128 or 256 (96 zero-padded to 128)   */
   int32_t page_size;         /* P: 8, 16, 32 or 64                              */
   int32_t max_pages_per_seq; /* row length of block_tables                       */
   int32_t num_pages;         /* pages in each cache tensor                       */
@@ -564,6 +564,7 @@ mcp_status mcp_mixed_attn_fwd_varlen(const mcp_plan* plan, const void* q, const 
 #define MCP_DEVERR_PAGE_RANGE 0x2   /* a block-table page id outside the pool    */
 #define MCP_DEVERR_SLOT_RANGE 0x4   /* an append slot outside the pool           */
 #define MCP_DEVERR_ROW_RANGE 0x8    /* a gathered row index outside the source   */
+#define MCP_DEVERR_ITEM_KIND 0x10   /* a work item this head_dim has no path for */
 
 #ifdef __cplusplus
 }

@@ -7,7 +7,8 @@
 // plan:
 //
 //  * tensor-core item -- 128 query rows (the G query heads of one kv head
-//    packed with 128/G tokens) against a KV range in 128-key tiles.  Warp 0
+//    packed with 128/G tokens) against a KV range in 128-key tiles (64 at
+//    head_dim 256).  Warp 0
 //    loads the Q tile with TMA and then issues O += P V; warp 1 issues
 //    S = Q K^T (A = Q, copied once into TMEM by the softmax warps; B = the K
 //    tile in shared memory); warps 6-9 load each K/V tile box by box through
@@ -29,7 +30,9 @@
 // head_dim 96 runs the D = 128 instantiation on 96-wide tensors: the tensor
 // maps span 96 columns, TMA fills columns 96-127 of every box with zeros, V
 // and decode stages take one box per 64-column panel, and only 96 columns of
-// O are stored.
+// O are stored.  head_dim 256 uses 64-key tiles (TMEM: S twice in columns
+// 0-127, O in 128-383, Q in 384-511) with two K and V stages, and has no
+// decode path: the planner gives its decode tokens tensor-core tiles.
 //
 // A split KV range writes (O, LSE) partials that combine.cu merges.
 //
@@ -65,12 +68,20 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 template <int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;        // 64-column (128-byte) swizzle panels
-  static constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 B
-  // tensor-core item
-  static constexpr int kQBytes = kHalves * kHalfBytes;
-  static constexpr int kKvBytes = kHalves * kHalfBytes;  // one K (or V) tile of 128 keys
-  static constexpr int kKStages = 3;  // K and V tiles of tile t share stage t % 3,
-  static constexpr int kVStages = 3;  // released together once P V(t) is done
+  // tensor-core item: 128-key tiles up to D = 128; at D = 256 64-key tiles,
+  // so that S (twice), O and Q fit the 512 TMEM columns and two K and V
+  // stages fit shared memory
+  static constexpr int kKvTile = D > 128 ? 64 : 128;
+  static constexpr int kQPanel = kTileRows * 128;  // a 64-column panel of Q: 128 rows x 128 B
+  static constexpr int kKPanel = kKvTile * 128;    // a 64-column panel of a K tile
+  static constexpr int kQBytes = kHalves * kQPanel;
+  static constexpr int kKvBytes = kHalves * kKPanel;  // one K (or V) tile
+  static constexpr int kKStages = D > 128 ? 2 : 3;  // K of tile t in stage t % kKStages
+  static constexpr int kVStages = kKStages;         // V of tile t in stage t % kVStages
+  // TMEM columns: S buffers [0, 2 kKvTile), O [kColO, kColO + D), Q [kColQ, kColQ + D/2)
+  static constexpr int kColO = 2 * kKvTile;
+  static constexpr int kColQ = 384;
+  static_assert(kColO + D <= kColQ && kColQ + D / 2 <= 512, "TMEM columns");
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kQBytes;                          // K stage s at kOffK + s*kKvBytes
   static constexpr int kOffV = kOffK + kKStages * kKvBytes;      // V stage s at kOffV + s*kKvBytes
@@ -221,6 +232,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                              int warp, int lane) {
   using C = Cfg<D>;
+  constexpr int kKvTile = C::kKvTile;  // keys per tile (shadows the 128 of the planner)
   const int G = p.G;
   const int TQ = kTileRows / G;
   const int kv0 = it.kv_begin, kv1 = it.kv_end;
@@ -241,12 +253,12 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(c.b(BQ), C::kHalves * G * TQ * 128);
       for (int h = 0; h < C::kHalves; ++h)
-        ptx::tma_load_3d(sQ + h * C::kHalfBytes, tm_q, c.b(BQ), 64 * h, it.kv_head * G,
+        ptx::tma_load_3d(sQ + h * C::kQPanel, tm_q, c.b(BQ), 64 * h, it.kv_head * G,
                          sg.q_start + it.q_begin, ptx::policy_evict_first());
     }
     __syncwarp();
-    const uint32_t tS = tmem;        // S buffers: columns [0,128) and [128,256)
-    const uint32_t tO = tmem + 256;  // O: columns [256, 256 + D)
+    const uint32_t tS = tmem;              // S buffers: columns [0, kKvTile), [kKvTile, 2 kKvTile)
+    const uint32_t tO = tmem + C::kColO;   // O
     // descriptor of stage 0 built once; an MMA adds a byte offset >> 4 to the
     // start-address field (shared addresses stay below 256 KB: no carry out)
     // V stage: boxes of B tokens, each [panel][B tokens][128 B]: 64-column
@@ -344,7 +356,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
             for (int i = 0; i < nu; ++i)
 #pragma unroll
               for (int h = 0; h < C::kHalves; ++h)
-                ptx::tma_load_4d(dst + h * C::kHalfBytes + (u0 + i) * B * 128, tm, bar, 64 * h,
+                ptx::tma_load_4d(dst + h * C::kKPanel + (u0 + i) * B * 128, tm, bar, 64 * h,
                                  it.kv_head, blk_tok(p, pgs[i]), blk_page(p, pgs[i]), pol);
           } else {
             const uint32_t dst = sV(s);
@@ -376,8 +388,8 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ Q K^T issuer
-    const uint32_t tS = tmem;        // S buffers: columns [0,128) and [128,256)
-    const uint32_t tQ = tmem + 384;  // Q: columns [384, 384 + D/2), two bf16 per column
+    const uint32_t tS = tmem;              // S buffers
+    const uint32_t tQ = tmem + C::kColQ;   // Q: D/2 columns, two bf16 per column
     const uint64_t dK0 = ptx::sdesc_sw128(sK(0), 16, 1024);
     bool ok = wait_on(c, c.b(BQT), 0);
     for (int t = 0; ok && t < ntiles; ++t) {
@@ -395,7 +407,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
         // A = Q from TMEM (loaded once per item), B = the K tile from shared memory
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          constexpr int kPanel = C::kHalfBytes;
+          constexpr int kPanel = C::kKPanel;
           ptx::mma_ts(ts, tQ + kk * 8, dk + (((kk >> 2) * kPanel + (kk & 3) * 32) >> 4), kIdQK,
                       kk > 0 ? 1u : 0u);
         }
@@ -413,7 +425,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     const int row = qw * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
     const uint32_t tS = tmem + lane_base;
-    const uint32_t tO = tmem + 256 + lane_base;
+    const uint32_t tO = tmem + C::kColO + lane_base;
     const int tok = it.q_begin + row / G;  // token index inside the segment
     const int g = row - (row / G) * G;
     const bool valid = row < G * TQ && tok < it.q_begin + it.q_count;
@@ -434,14 +446,14 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
-          const uint4 v = *reinterpret_cast<const uint4*>(qrow + h * C::kHalfBytes + ((ch ^ (row & 7)) << 4));
+          const uint4 v = *reinterpret_cast<const uint4*>(qrow + h * C::kQPanel + ((ch ^ (row & 7)) << 4));
           qv[h * 32 + ch * 4 + 0] = v.x;
           qv[h * 32 + ch * 4 + 1] = v.y;
           qv[h * 32 + ch * 4 + 2] = v.z;
           qv[h * 32 + ch * 4 + 3] = v.w;
         }
 #pragma unroll
-      for (int j = 0; j < D / 64; ++j) ptx::tmem_st32(tmem + 384 + lane_base + j * 32, qv + j * 32);
+      for (int j = 0; j < D / 64; ++j) ptx::tmem_st32(tmem + C::kColQ + lane_base + j * 32, qv + j * 32);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(c.b(BQT));
@@ -502,14 +514,15 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       l = l * alpha + sum;
       // P(t) goes to the first 64 columns of S buffer t & 1 (this thread's lane,
       // already read); P V(t-1) reads the other buffer, so no wait is needed here
-      ptx::tmem_st32(tS + s * kKvTile, r);
-      ptx::tmem_st32(tS + s * kKvTile + 32, r + 32);
+#pragma unroll
+      for (int j = 0; j < kKvTile / 64; ++j) ptx::tmem_st32(tS + s * kKvTile + j * 32, r + j * 32);
       if (t > 0 && __any_sync(0xffffffffu, rescale)) {
         // P V of the previous tile (issued by the other MMA warp) must be done
-        // before O is rescaled; its barrier (V stage (t-1) % 3) completes next
-        // only with P V(t+2), which needs P(t+2), so it is at most one phase off.
-        const int ps = (t - 1) % C::kKStages;
-        if (!(ok = wait_on_warp(c, c.b(BE0 + ps), ((t - 1) / C::kKStages) & 1))) break;
+        // before O is rescaled; its barrier (V stage (t-1) % kVStages) completes
+        // next only with P V(t-1+kVStages), which needs P of that tile, so it
+        // is at most one phase off.
+        const int ps = (t - 1) % C::kVStages;
+        if (!(ok = wait_on_warp(c, c.b(BE0 + ps), ((t - 1) / C::kVStages) & 1))) break;
         ptx::tc_fence_after();
 #pragma unroll 1
         for (int j = 0; j < D / 32; ++j) {
@@ -961,8 +974,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (prefill) {
     prefill_item<D>(c, it, sg, p, base, gb, *tmem_slot, &tm_q, &tm_k, &tm_v, warp, lane);
-  } else {
+  } else if constexpr (D <= 128) {
     decode_item<D>(c, it, sg, p, base, gb, &tm_kd, &tm_vd, warp, lane);
+  } else {
+    // the planner sends every segment of a D = 256 step through tensor-core tiles
+    if (threadIdx.x == 0) atomicOr(p.err, MCP_DEVERR_ITEM_KIND);
   }
 
   ptx::tc_fence_before();
@@ -1124,6 +1140,7 @@ int launch_mixed_attn(const FwdArgs& a, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (a.head_dim == 128 || a.head_dim == 96) return launch_fwd_d<128>(a, st);
   if (a.head_dim == 64) return launch_fwd_d<64>(a, st);
+  if (a.head_dim == 256) return launch_fwd_d<256>(a, st);
   snprintf(g_detail, sizeof(g_detail), "head_dim %d not built", a.head_dim);
   return -1;
 }

@@ -153,6 +153,10 @@ int launch_combine(const FwdArgs& a, void* stream) {
     combine_kernel<128><<<blocks, 256, 0, st>>>(
         a.combine, a.num_combine, a.combine_rows, a.cu_seqlens_q, a.part_o, a.part_lse,
         static_cast<__nv_bfloat16*>(a.out), a.lse, a.num_q_heads, G);
+  } else if (a.head_dim == 256) {
+    combine_kernel<256><<<blocks, 256, 0, st>>>(
+        a.combine, a.num_combine, a.combine_rows, a.cu_seqlens_q, a.part_o, a.part_lse,
+        static_cast<__nv_bfloat16*>(a.out), a.lse, a.num_q_heads, G);
   } else if (a.head_dim == 96) {
     combine_kernel<96><<<blocks, 256, 0, st>>>(
         a.combine, a.num_combine, a.combine_rows, a.cu_seqlens_q, a.part_o, a.part_lse,

@@ -65,8 +65,8 @@ mcp_status validate_desc(const mcp_attn_desc* d) {
   if (d->num_q_heads % d->num_kv_heads != 0)
     return fail(MCP_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
                 d->num_q_heads, d->num_kv_heads);
-  if (d->head_dim != 64 && d->head_dim != 96 && d->head_dim != 128)
-    return fail(MCP_ERR_UNSUPPORTED, "head_dim %d (built: 64, 96, 128)", d->head_dim);
+  if (d->head_dim != 64 && d->head_dim != 96 && d->head_dim != 128 && d->head_dim != 256)
+    return fail(MCP_ERR_UNSUPPORTED, "head_dim %d (built: 64, 96, 128, 256)", d->head_dim);
   if (d->page_size != 8 && d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
     return fail(MCP_ERR_UNSUPPORTED, "page_size %d (built: 8, 16, 32, 64)", d->page_size);
   if (d->num_q_heads / d->num_kv_heads > mcp::kTileRows)
@@ -138,12 +138,15 @@ std::vector<Unit> plan_units(const mcp_attn_desc& d, const int32_t* cu, const in
                              int32_t num_rows) {
   const int G = d.num_q_heads / d.num_kv_heads;
   const int TQ = mcp::kTileRows / G;
+  // the decode path is built up to head_dim 128; at 256 every segment takes
+  // tensor-core tiles (a decode token fills G of a tile's 128 rows)
+  const bool dec_ok = d.head_dim <= 128;
   std::vector<Unit> u;
   if (!rows) {
     for (int s = 0; s < d.num_seqs; ++s) {
       const int64_t lq = cu[s + 1] - cu[s];
       if (lq == 0) continue;
-      if (lq * G <= mcp::kDecodeMaxRows) {
+      if (dec_ok && lq * G <= mcp::kDecodeMaxRows) {
         u.push_back({s, 0, lq, true});
       } else {
         for (int64_t qb = 0; qb < lq; qb += TQ) u.push_back({s, qb, std::min<int64_t>(TQ, lq - qb), false});
@@ -156,7 +159,7 @@ std::vector<Unit> plan_units(const mcp_attn_desc& d, const int32_t* cu, const in
   for (int32_t i = 0; i < num_rows;) {
     const int32_t t = rows[i];
     while (cu[s + 1] <= t) ++s;
-    const bool dec = G <= mcp::kDecodeMaxRows;
+    const bool dec = dec_ok && G <= mcp::kDecodeMaxRows;
     const int64_t cap = dec ? dec_max : TQ;
     int32_t j = i + 1;
     while (j < num_rows && rows[j] == rows[j - 1] + 1 && rows[j] < cu[s + 1] && j - i < cap) ++j;

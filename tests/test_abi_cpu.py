@@ -405,3 +405,16 @@ def test_head_dim_96_plans_with_96_wide_partials():
     assert rows > 0
     assert p96.off_part_lse - p96.off_part_o >= rows * 96 * 4
     assert p96.off_part_lse - p96.off_part_o < rows * 128 * 4
+
+
+def test_head_dim_256_plans_without_decode_items():
+    """The decode path is built up to head_dim 128: at 256 every segment,
+    decodes included, becomes tensor-core tiles."""
+    d = base_desc(head_dim=256, sm_scale=1 / 16.0)
+    st, plan, items, _ = plan_host(d, CU, SK)
+    assert st == 0
+    assert plan.num_decode_items == 0
+    assert plan.num_prefill_items == plan.num_items > 0
+    kinds = items["kind"] if items.dtype.names else None
+    if kinds is not None:
+        assert (kinds == 1).all()

@@ -124,7 +124,7 @@ EDGE = {
 
 @pytest.mark.parametrize("case", sorted(EDGE))
 @pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (4, 4, 64), (16, 1, 128), (6, 2, 64),
-                                      (32, 8, 96), (12, 3, 96)])
+                                      (32, 8, 96), (12, 3, 96), (16, 4, 256), (8, 8, 256)])
 def test_edge_cases(case, hq, hkv, d):
     q, k = EDGE[case]
     w = synth.make_workload_from_lengths(case, hq, hkv, d, 16, 1 / math.sqrt(d), q, k, 1234)
@@ -241,7 +241,8 @@ def test_other_page_sizes(case, page_size):
     full_parity(w, options=opts(16, 128), label=f"{case}/p{page_size}/split")
 
 
-@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (6, 2, 64), (16, 1, 128), (32, 8, 96)])
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (6, 2, 64), (16, 1, 128), (32, 8, 96),
+                                      (16, 4, 256)])
 def test_page8_head_shapes(hq, hkv, d):
     """8-token pages with D = 64 (one 64-column panel), D = 96 (one box per
     panel) and other head groups."""
@@ -250,3 +251,15 @@ def test_page8_head_shapes(hq, hkv, d):
                                          q, k, 99)
     full_parity(w, label=f"p8/{hq}/{hkv}/{d}")
     full_parity(w, options=opts(16, 128), label=f"p8/{hq}/{hkv}/{d}/split")
+
+
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_head_dim_256_mixed_step(page_size):
+    """head_dim 256: 64-key tiles and every segment (decodes included) on the
+    tensor-core path; several tiles per item, a ragged tail and splits."""
+    q = [1, 1, 3, 300, 1]
+    k = [121, 4000, 700, 300 + 2500, 65]
+    w = synth.make_workload_from_lengths(f"d256-p{page_size}", 16, 4, 256, page_size,
+                                         1 / math.sqrt(256), q, k, 256)
+    full_parity(w, label=f"d256/p{page_size}")
+    full_parity(w, options=opts(16, 128), label=f"d256/p{page_size}/split")
