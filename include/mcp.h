@@ -61,7 +61,7 @@ extern "C" {
 typedef enum mcp_status {
   MCP_OK = 0,
   MCP_ERR_INVALID_ARG = 1,         /* bad pointer, size, layout or metadata        */
-  MCP_ERR_UNSUPPORTED = 2,         /* valid but not built (e.g. head_dim 96)       */
+  MCP_ERR_UNSUPPORTED = 2,         /* valid but not built (e.g. head_dim 80)       */
   MCP_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace smaller than the plan needs        */
   MCP_ERR_CUDA = 4,                /* a CUDA runtime/driver call failed            */
   MCP_ERR_TIMEOUT = 5,             /* a device-side bounded wait gave up           */
