@@ -200,7 +200,7 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
-    w = synth.make_workload(args.config)
+    w = synth.make_workload(args.config, head_dim=args.head_dim, page_size=args.page_size)
     cu0 = np.concatenate([[0], np.cumsum(w.q_lens)]).astype(np.int32)
     rows = mcp.build_logits_indices(cu0) if args.rows == "logits" else None
     alg = algorithmic(w, rows)
@@ -322,8 +322,8 @@ def run_gpu(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
-        "config": {"workload": synth.DESCRIPTIONS[args.config], "name": args.config,
-                   "segments": w.num_seqs, "total_q": w.total_q,
+        "config": {"workload": synth.describe(args.config, args.head_dim, args.page_size),
+                   "name": args.config, "segments": w.num_seqs, "total_q": w.total_q,
                    "kv_tokens": int(sum(w.k_lens)), "l2": "flushed between steps (256 MB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "step": "paged_kv_append + mixed_attn_fwd (+ combine)",
@@ -365,13 +365,13 @@ def oracle_cores():
 class OracleSample:
     """The oracle on one workload's inputs, restricted to a row sample."""
 
-    def __init__(self, name):
+    def __init__(self, name, head_dim=None, page_size=None):
         sys.path.insert(0, os.path.join(ROOT, "tests"))
         import torch
 
         from harness import OracleStep
 
-        w = synth.make_workload(name)
+        w = synth.make_workload(name, head_dim=head_dim, page_size=page_size)
         self.w = w
         if name in ("decode-heavy", "long-context"):
             # too large to hold whole: keep the chunk and two decodes
@@ -530,8 +530,8 @@ def run_serve(args):
             "chunked": out["chunked_512"], "unchunked": out["unchunked"]}
 
 
-def cpu_baseline(name, budget_s=15.0):
-    s = OracleSample(name)
+def cpu_baseline(name, budget_s=15.0, head_dim=None, page_size=None):
+    s = OracleSample(name, head_dim, page_size)
     rows = s.rows(4)
     dt = s.time_rows(rows)
     n = len(rows)
@@ -547,7 +547,7 @@ def cpu_baseline(name, budget_s=15.0):
 
 
 def run_reference(args):
-    s = OracleSample(args.config)
+    s = OracleSample(args.config, args.head_dim, args.page_size)
     budget = 150.0
     per_step = budget / max(1, args.steps + args.warmup)
     rows = s.rows(2)
@@ -567,7 +567,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
-            "config": {"workload": synth.DESCRIPTIONS[args.config], "name": args.config},
+            "config": {"workload": synth.describe(args.config, args.head_dim, args.page_size),
+                       "name": args.config},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_cores(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -580,6 +581,10 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="worked", choices=synth.CONFIG_NAMES + synth.PROFILE_NAMES)
+    ap.add_argument("--head-dim", type=int, default=None, choices=[64, 96, 128, 256],
+                    help="run the workload's segments at this head_dim")
+    ap.add_argument("--page-size", type=int, default=None, choices=[8, 16, 32, 64],
+                    help="run the workload's segments with this page size")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -618,7 +623,8 @@ def main():
     res = run_gpu(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1 and args.rows == "all":
-            res["cpu_baseline"] = cpu_baseline(args.config)
+            res["cpu_baseline"] = cpu_baseline(args.config, head_dim=args.head_dim,
+                                               page_size=args.page_size)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

@@ -169,8 +169,32 @@ def make_workload_from_lengths(name, num_q_heads, num_kv_heads, head_dim, page_s
     return w
 
 
-def make_workload(name: str, seed_offset: int = 0) -> Workload:
-    """One of the named workloads, seeded with SEED_BASE + its index."""
+def make_workload(name: str, seed_offset: int = 0, head_dim: int | None = None,
+                  page_size: int | None = None) -> Workload:
+    """One of the named workloads, seeded with SEED_BASE + its index; with
+    head_dim / page_size the same segments and heads at that head dim
+    (sm_scale 1/sqrt(head_dim)) or page size."""
+    w = _named_workload(name, seed_offset)
+    if head_dim is None and page_size is None:
+        return w
+    d = int(head_dim or w.head_dim)
+    P = int(page_size or w.page_size)
+    return make_workload_from_lengths(f"{name}-d{d}-p{P}", w.num_q_heads, w.num_kv_heads, d, P,
+                                      1.0 / math.sqrt(d), w.q_lens, w.k_lens, w.seed)
+
+
+def describe(name: str, head_dim: int | None = None, page_size: int | None = None) -> str:
+    """DESCRIPTIONS[name], with the head_dim / page_size overrides stated."""
+    text = DESCRIPTIONS[name]
+    over = []
+    if head_dim is not None:
+        over.append(f"head_dim {int(head_dim)}")
+    if page_size is not None:
+        over.append(f"page {int(page_size)}")
+    return text + (" -- here with " + ", ".join(over) if over else "")
+
+
+def _named_workload(name: str, seed_offset: int = 0) -> Workload:
     if name in PROFILE_NAMES:
         seed = SEED_BASE + 100 + PROFILE_NAMES.index(name) + seed_offset
         if name == "decode-32x16k":
