@@ -585,7 +585,7 @@ def main():
     ap.add_argument("--config", default="worked", choices=synth.CONFIG_NAMES + synth.PROFILE_NAMES)
     ap.add_argument("--head-dim", type=int, default=None, choices=[64, 96, 128, 256],
                     help="run the workload's segments at this head_dim")
-    ap.add_argument("--page-size", type=int, default=None, choices=[8, 16, 32, 64],
+    ap.add_argument("--page-size", type=int, default=None, choices=[1, 8, 16, 32, 64],
                     help="run the workload's segments with this page size")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)

@@ -128,7 +128,7 @@ typedef struct mcp_attn_desc {
   int32_t num_q_heads;       /* H_q                                              */
   int32_t num_kv_heads;      /* H_kv; must divide H_q                            */
   int32_t head_dim;          /* D: 64, 96, 128 or 256 (96 zero-padded to 128)   */
-  int32_t page_size;         /* P: 8, 16, 32 or 64                              */
+  int32_t page_size;         /* P: 1, 8, 16, 32 or 64                           */
   int32_t max_pages_per_seq; /* row length of block_tables                       */
   int32_t num_pages;         /* pages in each cache tensor                       */
   float sm_scale;            /* score scale > 0, e.g. 1/sqrt(D) ([K] kernel launch) */
@@ -405,7 +405,7 @@ typedef struct mcp_sched_config {
   int32_t long_prefill_token_threshold; /* 0 = none, else max tokens of one chunk    */
   int32_t max_num_seqs;                 /* segments in one step (>= 1)               */
   int32_t num_pages;                    /* device KV pool pages                      */
-  int32_t page_size;                    /* tokens per page (8, 16, 32 or 64)         */
+  int32_t page_size;                    /* tokens per page (1, 8, 16, 32 or 64)      */
   int32_t max_pages_per_seq;            /* block-table row length                    */
   int32_t preempt_swap;                 /* 0 = recompute, 1 = swap to the host pool  */
   int32_t num_host_pages;               /* host swap pool pages (swap mode)          */

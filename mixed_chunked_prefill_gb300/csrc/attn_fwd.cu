@@ -186,6 +186,10 @@ struct KParams {
   int32_t dr;          // head_dim of the tensors (row width of q, out, K/V, partials): the
                        // kernel's D, or 96 run as D = 128 (TMA fills columns 96-127 with 0)
   int32_t panel_boxes; // 1: V and decode boxes cover one 64-column panel each (dr < D)
+  int32_t gather;      // 1: 1-token pages; the producers gather K/V rows with cp.async
+  int32_t hkv;         // kv heads (row stride of the caches, in head_dim rows)
+  const __nv_bfloat16* kc;  // caches [num_pages, 1, H_kv, dr] (gather only)
+  const __nv_bfloat16* vc;
   const int32_t* cu_k; // non-paged K/V: first row of each segment's keys (else nullptr)
   float scale_log2;    // sm_scale * log2(e): scores live in log2 units
 };
@@ -309,6 +313,69 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     __syncwarp();
     drain_wait(c.abort, c.err, c.b(BDRAIN), 0);
     drain_wait(c.abort, c.err, c.b(BQ), 0);
+  } else if (warp >= 6 && p.gather) {
+    // ------------------- K/V producers for 1-token pages: cp.async gathers
+    // Every key is its own page, so a TMA box would carry one 128-byte row;
+    // instead 64 threads per operand (warps 6-7: K, 8-9: V) copy whole key
+    // rows in 16-byte pieces into the same swizzled layouts the TMA path
+    // fills: K [panel][key][128 B], V [16-key block][panel][16 keys][128 B],
+    // 16-byte chunk ch of row r at (ch ^ (r % 8)) * 16.  A thread commits one
+    // copy group per tile and, once the group of the tile before has landed,
+    // makes it visible to the tensor core (proxy fence) and arrives on that
+    // tile's barrier (64 arrivals), keeping two tiles in flight.
+    const int pr = warp - 6;
+    const bool isK = pr < 2;
+    const int tid = (pr & 1) * 32 + lane;
+    const __nv_bfloat16* cache = isK ? p.kc : p.vc;
+    const int NS = C::kKStages;
+    const int full0 = isK ? BK0 : BV0, empty0 = isK ? BKE0 : BE0;
+    constexpr int kKeysPer = kKvTile / 64;  // keys of a tile per thread
+    constexpr int kChunks = D / 8;          // 16-byte pieces of a key row
+    const size_t head_off = static_cast<size_t>(it.kv_head) * p.dr;
+    const size_t page_elems = static_cast<size_t>(p.hkv) * p.dr;  // one token per page
+    int t = 0;
+    for (; t < ntiles; ++t) {
+      const int s = t % NS;
+      if (t >= NS && !wait_on(c, c.b(empty0 + s), ((t / NS) + 1) & 1)) break;
+      const uint32_t stage = isK ? sK(s) : sV(s);
+#pragma unroll
+      for (int j = 0; j < kKeysPer; ++j) {
+        const int key = tid + 64 * j;
+        const int pos = kv0 + t * kKvTile + key;
+        int page = -1;
+        if (pos < kv1) {
+          const int v = p.bt[static_cast<size_t>(it.seg) * p.max_pages + pos];
+          if (v >= 0 && v < p.num_pages) page = v;
+          else atomicOr(p.err, MCP_DEVERR_PAGE_RANGE);
+        }
+        const __nv_bfloat16* row =
+            page >= 0 ? cache + static_cast<size_t>(page) * page_elems + head_off : cache;
+        const uint32_t swz = static_cast<uint32_t>(key & 7);
+        const uint32_t kbase = stage + key * 128;
+        const uint32_t vbase = stage + (key >> 4) * C::kHeadBlock + (key & 15) * 128;
+#pragma unroll
+        for (int cc = 0; cc < kChunks; ++cc) {
+          const int panel = cc >> 3;
+          const uint32_t ch = static_cast<uint32_t>(cc & 7);
+          const uint32_t dst = (isK ? kbase + panel * C::kKPanel : vbase + panel * kPageSize * 128) +
+                               ((ch ^ swz) << 4);
+          // keys past the item and columns past head_dim are written as zeros
+          const bool in = page >= 0 && cc * 8 < p.dr;
+          ptx::cp_async16(dst, in ? row + cc * 8 : cache, in ? 16u : 0u);
+        }
+      }
+      ptx::cp_async_commit();
+      if (t > 0) {
+        ptx::cp_async_wait_group<1>();  // the copies of tile t - 1 have landed
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(c.b(full0 + (t - 1) % NS));
+      }
+    }
+    ptx::cp_async_wait_group<0>();
+    if (t > 0) {
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(c.b(full0 + (t - 1) % NS));
+    }
   } else if (warp >= 6) {
     // -------------------------------------- K/V producers: four warps
     // warp 6: K boxes of keys 0-63, warp 7: K keys 64-127, warp 8: V keys 0-63,
@@ -940,7 +1007,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;
-      if (i >= BK0 && i < BV0 + 3) count = 2;          // two producer warps per K / V tile
+      if (i >= BK0 && i < BV0 + 3) count = p.gather ? 64 : 2;  // producer warps (threads) per tile
       if (i == BP0 || i == BP0 + 1 || i == BQT) count = 128;  // every softmax thread
       if (i == BDRAIN) count = 2;                       // the Q K^T and the P V issuer
       if (i >= BEMPTY0) count = prefill ? 1 : it.num_heads;  // one warp per head reads a stage
@@ -1068,7 +1135,10 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   const cuuint64_t npages = contig ? 1 : static_cast<cuuint64_t>(a.num_pages);
   const cuuint64_t page_stride = ntok * a.num_kv_heads * dr2;
   // tokens per TMA box: 8 for page size 8, else 16 (a larger page is several boxes)
-  const int box_tok = (!contig && a.page_size == 8) ? 8 : kPageSize;
+  // (1-token pages: the maps are encoded with 1-token boxes but the producers
+  // gather with cp.async and the shared-memory layout is the 16-token one)
+  const bool gather = !contig && a.page_size == 1;
+  const int box_tok = gather ? 1 : (!contig && a.page_size == 8) ? 8 : kPageSize;
   const bool panel_boxes = dr != D;
   {
     // one 64-column panel of one kv head of box_tok tokens: dims {d, head, token, page}
@@ -1115,6 +1185,10 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   kp.max_pages = a.max_pages_per_seq;
   kp.spp_log2 = contig ? 0 : (a.page_size == 64 ? 2 : (a.page_size == 32 ? 1 : 0));
   kp.box_log2 = box_tok == 8 ? 3 : 4;
+  kp.gather = gather ? 1 : 0;
+  kp.hkv = a.num_kv_heads;
+  kp.kc = static_cast<const __nv_bfloat16*>(a.k_cache);
+  kp.vc = static_cast<const __nv_bfloat16*>(a.v_cache);
   kp.dr = dr;
   kp.panel_boxes = panel_boxes ? 1 : 0;
   kp.cu_k = a.cu_seqlens_k;

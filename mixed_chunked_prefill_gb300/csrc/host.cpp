@@ -67,8 +67,9 @@ mcp_status validate_desc(const mcp_attn_desc* d) {
                 d->num_q_heads, d->num_kv_heads);
   if (d->head_dim != 64 && d->head_dim != 96 && d->head_dim != 128 && d->head_dim != 256)
     return fail(MCP_ERR_UNSUPPORTED, "head_dim %d (built: 64, 96, 128, 256)", d->head_dim);
-  if (d->page_size != 8 && d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
-    return fail(MCP_ERR_UNSUPPORTED, "page_size %d (built: 8, 16, 32, 64)", d->page_size);
+  if (d->page_size != 1 && d->page_size != 8 && d->page_size != 16 && d->page_size != 32 &&
+      d->page_size != 64)
+    return fail(MCP_ERR_UNSUPPORTED, "page_size %d (built: 1, 8, 16, 32, 64)", d->page_size);
   if (d->num_q_heads / d->num_kv_heads > mcp::kTileRows)
     return fail(MCP_ERR_UNSUPPORTED, "group size %d > 128", d->num_q_heads / d->num_kv_heads);
   if (d->num_kv_heads > 32767)
@@ -138,9 +139,10 @@ std::vector<Unit> plan_units(const mcp_attn_desc& d, const int32_t* cu, const in
                              int32_t num_rows) {
   const int G = d.num_q_heads / d.num_kv_heads;
   const int TQ = mcp::kTileRows / G;
-  // the decode path is built up to head_dim 128; at 256 every segment takes
-  // tensor-core tiles (a decode token fills G of a tile's 128 rows)
-  const bool dec_ok = d.head_dim <= 128;
+  // the decode path is built up to head_dim 128 and for pages of 8 or more
+  // tokens; at head_dim 256 or 1-token pages every segment takes tensor-core
+  // tiles (a decode token fills G of a tile's 128 rows)
+  const bool dec_ok = d.head_dim <= 128 && d.page_size >= 8;
   std::vector<Unit> u;
   if (!rows) {
     for (int s = 0; s < d.num_seqs; ++s) {

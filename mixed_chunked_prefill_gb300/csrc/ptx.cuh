@@ -88,6 +88,21 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* m, 
       "l"(policy)
       : "memory");
 }
+// 16-byte global -> shared copy (cp.async, bypassing L1); src_bytes 0 reads
+// nothing and writes zeros.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed copy groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {

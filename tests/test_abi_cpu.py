@@ -418,3 +418,20 @@ def test_head_dim_256_plans_without_decode_items():
     kinds = items["kind"] if items.dtype.names else None
     if kinds is not None:
         assert (kinds == 1).all()
+
+
+def test_page_size_1_plans_tiles_and_slot_mapping():
+    """1-token pages: every segment becomes tensor-core tiles (the decode path
+    is built for pages of 8 or more tokens); slots follow the oracle."""
+    w16 = synth.make_workload("worked")
+    w = synth.make_workload("worked", page_size=1)
+    cu, _, _, _ = oracle.segment_layout(w.q_lens, w.k_lens)
+    st, plan, items, _ = plan_host(desc_for(w), cu, w.k_lens)
+    assert st == 0 and plan.num_decode_items == 0 and plan.num_prefill_items == plan.num_items
+    st16, plan16, _, _ = plan_host(desc_for(w16), cu, w16.k_lens)
+    assert plan.num_items == plan16.num_items - plan16.num_decode_items + 2 * w.num_kv_heads
+    bt = w.block_tables()
+    table = oracle.page_table_from_block_tables(bt, w.k_lens, 1)
+    want = oracle.new_token_slots(table, cu, w.k_lens)
+    got = mcp.build_slot_mapping(bt, cu, w.k_lens, 1, w.num_pages)
+    assert np.array_equal(got, want)

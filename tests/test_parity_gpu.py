@@ -231,7 +231,7 @@ BIG_PAGE_CASES = {
 }
 
 
-@pytest.mark.parametrize("page_size", [8, 32, 64])
+@pytest.mark.parametrize("page_size", [1, 8, 32, 64])
 @pytest.mark.parametrize("case", sorted(BIG_PAGE_CASES))
 def test_other_page_sizes(case, page_size):
     q, k = BIG_PAGE_CASES[case]
@@ -263,3 +263,14 @@ def test_head_dim_256_mixed_step(page_size):
                                          1 / math.sqrt(256), q, k, 256)
     full_parity(w, label=f"d256/p{page_size}")
     full_parity(w, options=opts(16, 128), label=f"d256/p{page_size}/split")
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (32, 8, 96), (16, 4, 256), (16, 1, 128)])
+def test_page1_head_shapes(hq, hkv, d):
+    """1-token pages: K/V rows gathered with cp.async, every segment on
+    tensor-core tiles; other head dims and head groups."""
+    q, k = BIG_PAGE_CASES["mixed"]
+    w = synth.make_workload_from_lengths(f"p1-{hq}-{hkv}-{d}", hq, hkv, d, 1, 1 / math.sqrt(d),
+                                         q, k, 11)
+    full_parity(w, label=f"p1/{hq}/{hkv}/{d}")
+    full_parity(w, options=opts(16, 128), label=f"p1/{hq}/{hkv}/{d}/split")
