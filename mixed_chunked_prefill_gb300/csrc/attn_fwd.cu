@@ -32,7 +32,9 @@
 // and decode stages take one box per 64-column panel, and only 96 columns of
 // O are stored.  head_dim 256 uses 64-key tiles (TMEM: S twice in columns
 // 0-127, O in 128-383, Q in 384-511) with two K and V stages, and has no
-// decode path: the planner gives its decode tokens tensor-core tiles.
+// decode path: the planner gives its decode tokens tensor-core tiles.  With
+// 1-token pages the producers gather K/V rows with cp.async into the same
+// layouts (and decode tokens take tensor-core tiles too).
 //
 // A split KV range writes (O, LSE) partials that combine.cu merges.
 //
