@@ -134,51 +134,88 @@ def profiled_traffic(workload):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 20 ms from start() to stop(); the summary is
+    taken over the samples whose timestamps fall between mark_begin() and
+    mark_end() (the timed region), or over all samples, labelled, when the
+    region was too short to catch one."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.out = None
+        self.t_begin = self.t_end = None
 
     def start(self):
         try:
-            self.out = open(os.devnull if False else "/tmp/_mcp_clocks_%d.csv" % os.getpid(), "w")
+            self.out = open("/tmp/_mcp_clocks_%d.csv" % os.getpid(), "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
+    def mark_begin(self):
+        self.t_begin = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    @staticmethod
+    def parse(lines):
+        """(epoch seconds or None, sm MHz, max MHz, [reason names]) per CSV line."""
+        import datetime
+
+        out = []
+        for line in lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            try:
+                sm, mx = float(parts[2]), float(parts[3])
+            except ValueError:
+                continue
+            reasons = [ClockSampler.REASONS[i] for i in range(4)
+                       if parts[6 + i].lower() == "active"]
+            out.append((ts, sm, mx, reasons))
+        return out
+
+    def summary(self, samples):
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        inside = [x for x in samples if x[0] is not None and self.t_begin is not None
+                  and self.t_end is not None and self.t_begin <= x[0] <= self.t_end]
+        use = inside or samples
+        return {"sm_mhz": statistics.median(x[1] for x in use),
+                "sm_max_mhz": max(x[2] for x in samples),
+                "reasons": sorted({r for x in use for r in x[3]}),
+                "samples": len(samples), "samples_in_region": len(inside),
+                "window": "timed region" if inside else
+                          "whole run (the timed region was shorter than the 20 ms sampling)"}
+
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.out.close()
-        rows = []
         with open(self.out.name) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+            lines = f.readlines()
         os.unlink(self.out.name)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+        return self.summary(self.parse(lines))
 
 
 # ---------------------------------------------------------------------------
@@ -254,6 +291,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)
+    clocks.mark_begin()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
             flush.fill_(float(i))
@@ -264,6 +302,7 @@ def run_gpu(args, rank, world, local_rank):
             fwd_evs[i][1].record(stream)
             evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark_end()
     clk = clocks.stop()
     step.check()
     step_ms = [a.elapsed_time(b) for a, b in evs]

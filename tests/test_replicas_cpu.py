@@ -64,3 +64,32 @@ def test_single_rank_needs_no_collective():
 
     assert bench.max_over_ranks(7.5, 1, "cpu") == 7.5
     assert bench.job_rate(100, 1, 2.0) == 50.0
+
+
+def test_clock_samples_are_summarised_over_the_timed_region():
+    """The bench's nvidia-smi summary keeps the samples inside the timed
+    region (median SM clock, throttle reasons seen there) and falls back to
+    every sample, labelled, when the region caught none."""
+    import datetime
+
+    import bench
+
+    def line(t, sm, cap):
+        ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return (f"{ts}, 0, {sm}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, "
+                f"{'Active' if cap else 'Not Active'}\n")
+
+    t0 = 1_800_000_000.0
+    lines = [line(t0 + 0.00, 2070, False), line(t0 + 0.02, 1980, True),
+             line(t0 + 0.04, 2010, True), line(t0 + 0.06, 2070, False), "garbage\n"]
+    c = bench.ClockSampler(0)
+    samples = c.parse(lines)
+    assert len(samples) == 4
+    c.t_begin, c.t_end = t0 + 0.01, t0 + 0.05
+    s = c.summary(samples)
+    assert s["samples_in_region"] == 2 and s["sm_mhz"] == 1995.0
+    assert s["reasons"] == ["sw_power_cap"] and s["sm_max_mhz"] == 2070.0
+    c.t_begin, c.t_end = t0 + 0.07, t0 + 0.08
+    s = c.summary(samples)
+    assert s["samples_in_region"] == 0 and s["sm_mhz"] == 2040.0 and "whole run" in s["window"]
+    assert c.summary([])["samples"] == 0
