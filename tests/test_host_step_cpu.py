@@ -77,3 +77,15 @@ def test_create_and_calls_reject_null_before_cuda():
                                  None, ctypes.byref(t)) == 1
     assert lib.mcp_host_step_wait(None, 0) == 1
     assert lib.mcp_host_step_destroy(None) == 0
+
+
+@pytest.mark.parametrize("d,p", [(64, 16), (96, 16), (256, 16), (128, 1), (128, 8), (256, 64)])
+def test_arena_bytes_for_every_built_shape(d, p):
+    """Every built head_dim / page size sizes its arenas; the device arena
+    grows with head_dim (q, out, k_new, v_new rows of 2 * d bytes)."""
+    T = 1024
+    st, dbytes, hbytes = sizes(shape(d=d, p=p, scale=1.0 / d ** 0.5), limits(T, 32, 2048))
+    assert st == 0 and dbytes % 256 == 0 and hbytes % 256 == 0
+    assert dbytes >= 2 * T * (2 * 32 + 2 * 8) * d * 2
+    st64, d64, _ = sizes(shape(d=64, p=p), limits(T, 32, 2048))
+    assert st64 == 0 and (d == 64 or dbytes > d64)
