@@ -999,6 +999,7 @@ struct mcp_host_step {
   cudaStream_t compute = nullptr, h2d = nullptr, d2h = nullptr;
   Slot slot[2];
   int64_t next = 0;
+  std::vector<int64_t> slots_tmp;  // the next step's slot mapping, built before its slot is free
 
   // Wait for the slot's step and turn its device error word into a status.
   mcp_status settle(Slot& sl) {
@@ -1102,18 +1103,16 @@ mcp_status mcp_host_step_run(mcp_host_step* step, int32_t num_seqs, const int32_
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16))
       return fail(MCP_ERR_INVALID_ARG, "caches must be 16-byte aligned");
 
-    mcp_host_step::Slot& sl = step->slot[step->next & 1];
-    // the slot's previous step must be finished before its buffers are reused
-    mcp_status st = step->settle(sl);
-    if (st != MCP_OK) return st;
-
+    // Plan and build the slot mapping (which validates every page id) before
+    // waiting for this step's slot: the slot frees when the step two before
+    // has copied its output out, and the host work then overlaps it.
     mcp_attn_desc desc = step->shape;
     desc.num_seqs = num_seqs;
     desc.total_q = T;
     desc.max_pages_per_seq = lim.max_pages_per_seq;
     mcp_plan plan;
     Built b;
-    st = plan_common(&desc, cu_seqlens_q, seqlens_k, nullptr, &plan, b);
+    mcp_status st = plan_common(&desc, cu_seqlens_q, seqlens_k, nullptr, &plan, b);
     if (st != MCP_OK) return st;
     if (plan.workspace_bytes > L.ws_bytes)
       return fail(MCP_ERR_WORKSPACE_TOO_SMALL, "step needs %lld workspace bytes > limit %lld",
@@ -1121,13 +1120,20 @@ mcp_status mcp_host_step_run(mcp_host_step* step, int32_t num_seqs, const int32_
     if (plan.off_part_o > L.list_bytes)
       return fail(MCP_ERR_WORKSPACE_TOO_SMALL, "work lists need %lld bytes > limit %lld",
                   static_cast<long long>(plan.off_part_o), static_cast<long long>(L.list_bytes));
-    // host staging: metadata, slot mapping (validates every page id), work lists
     const int64_t S = num_seqs, mp = lim.max_pages_per_seq;
+    step->slots_tmp.resize(static_cast<size_t>(std::max(1, T)));
+    st = mcp_build_slot_mapping(block_tables, num_seqs, lim.max_pages_per_seq, desc.page_size,
+                                desc.num_pages, cu_seqlens_q, seqlens_k, step->slots_tmp.data());
+    if (st != MCP_OK) return st;
+
+    mcp_host_step::Slot& sl = step->slot[step->next & 1];
+    // the slot's previous step must be finished before its buffers are reused
+    st = step->settle(sl);
+    if (st != MCP_OK) return st;
+    // host staging: metadata, slot mapping, work lists
     int32_t* hm = reinterpret_cast<int32_t*>(sl.host + L.h_meta);
     int64_t* hs = reinterpret_cast<int64_t*>(sl.host + L.h_slots);
-    st = mcp_build_slot_mapping(block_tables, num_seqs, lim.max_pages_per_seq, desc.page_size,
-                                desc.num_pages, cu_seqlens_q, seqlens_k, hs);
-    if (st != MCP_OK) return st;
+    if (T > 0) std::memcpy(hs, step->slots_tmp.data(), static_cast<size_t>(T) * sizeof(int64_t));
     std::memcpy(hm, cu_seqlens_q, (S + 1) * sizeof(int32_t));
     if (S > 0) {
       std::memcpy(hm + S + 1, seqlens_k, S * sizeof(int32_t));
