@@ -242,7 +242,8 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
     if (pre_ns > 0.0 && dec_ns < 0.1 * (pre_ns + dec_ns)) {
       // items of a candidate split (same for every candidate that splits no
       // unit differently); evaluating only distinct candidates and none past
-      // eight items per SM keeps the search to a few list schedules
+      // sixteen items per SM keeps the search to a few list schedules (finer
+      // splits than that only add per-item cost in this model)
       auto signature = [&](int64_t cand_ps) {
         uint64_t sig = 1469598103934665603ull;  // FNV-1a over the units' split counts
         for (const Unit& x : units) {
@@ -287,7 +288,9 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
       int64_t best = ps, last_sig = -1;
       double best_t = t0;
       for (int64_t cand = 65536; cand >= 2048; cand /= 2) {
-        if (count(ds, cand) > 8LL * std::max(1, num_sms)) break;  // counts grow as cand shrinks
+        // candidates finer than the rule's split stop past sixteen items per SM
+        // (counts grow as cand shrinks); coarser ones are always evaluated
+        if (cand < ps && count(ds, cand) > 16LL * std::max(1, num_sms)) break;
         const int64_t sig = signature(cand);
         if (sig == last_sig) continue;  // the previous, larger candidate had the same items
         last_sig = sig;

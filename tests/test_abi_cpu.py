@@ -435,3 +435,78 @@ def test_page_size_1_plans_tiles_and_slot_mapping():
     want = oracle.new_token_slots(table, cu, w.k_lens)
     got = mcp.build_slot_mapping(bt, cu, w.k_lens, 1, w.num_pages)
     assert np.array_equal(got, want)
+
+
+def _exhaustive_chunk_split(q_lens, k_lens, hq, hkv, d, num_sms):
+    """The split size an exhaustive list-scheduling search picks for a step of
+    chunks only: the planner's cost model (per item ~5 us + ~0.75 us per
+    128-key tile at D = 128, longest item first onto the least-loaded SM),
+    every candidate from 65536 down to 2048 evaluated, ties within 2% to the
+    larger split.  Returns (split, items of that split)."""
+    import heapq
+
+    G = hq // hkv
+    TQ = 128 // G
+
+    def cdiv(a, b):
+        return -(-a // b)
+
+    def even_split(length, cap, gran):
+        k = max(1, cdiv(length, cap))
+        sz = cdiv(cdiv(length, k), gran) * gran
+        return cdiv(length, sz), sz
+
+    vis = []
+    for lq, lk in zip(q_lens, k_lens):
+        assert lq * G > 16  # chunks only: no decode units
+        for qb in range(0, lq, TQ):
+            vis.append(lk - lq + qb + min(TQ, lq - qb))
+    count = lambda ps: sum(even_split(v, ps, 128)[0] for v in vis) * hkv
+    ps = 32768
+    while count(ps) < 2 * num_sms and ps > 2048:
+        ps //= 2
+    tile_ns, item_ns = 750.0 * d / 128.0, 5000.0
+
+    def makespan(cand):
+        cost = []
+        for v in vis:
+            n, sz = even_split(v, cand, 128)
+            for k in range(n):
+                c = item_ns + cdiv(min(sz, v - k * sz), 128) * tile_ns
+                cost += [c] * hkv
+        cost.sort(reverse=True)
+        load = [0.0] * num_sms
+        for c in cost:
+            heapq.heapreplace(load, load[0] + c)
+        return max(load)
+
+    best, best_t = ps, makespan(ps)
+    cand = 65536
+    while cand >= 2048:
+        t = makespan(cand)
+        if t < best_t * 0.98 or (t <= best_t * 1.02 and cand > best):
+            best_t = min(best_t, t)
+            best = cand
+        cand //= 2
+    return best, count(best)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_pruned_split_search_matches_exhaustive(seed):
+    """The planner evaluates only distinct split candidates and none past
+    sixteen items per SM; on chunk-only steps it picks what the exhaustive
+    search picks whenever that choice is within sixteen items per SM."""
+    rng = np.random.Generator(np.random.PCG64(5000 + seed))
+    num_sms = int(rng.choice([152, 148, 132, 100]))
+    hq, hkv = [(32, 8), (64, 8), (16, 16), (32, 4)][seed % 4]
+    nseg = int(rng.integers(1, 4))
+    q_lens = [int(x) for x in rng.integers(64, 2048, size=nseg)]
+    k_lens = [q + int(h) for q, h in zip(q_lens, rng.integers(0, 40000, size=nseg))]
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    mp = max(-(-k // 16) for k in k_lens)
+    d = mcp.make_desc(nseg, int(cu[-1]), hq, hkv, 128, 16, mp, mp * nseg + 1, 1 / math.sqrt(128))
+    st, plan, _, _ = plan_host(d, cu, k_lens, num_sms=num_sms)
+    assert st == 0
+    want, items = _exhaustive_chunk_split(q_lens, k_lens, hq, hkv, 128, num_sms)
+    if items <= 16 * num_sms:
+        assert plan.prefill_split_tokens == want, (q_lens, k_lens, num_sms, want)
