@@ -58,6 +58,7 @@ def run_random_traffic(s, reqs, steps, check_step=None):
     """Drive the scheduler; mirror every request's state from the plans and
     check the invariants the pages fix."""
     B, T_cap, thr, S_cap, pool = s._cfg
+    P = s._page
     state = {r: dict(prompt=pl, tokens=pl, computed=0, generated=0, max_new=mn, pages=[])
              for r, (pl, mn, pr) in reqs.items()}
     done = set()
@@ -111,10 +112,12 @@ def run_random_traffic(s, reqs, steps, check_step=None):
 
 
 class Sched(Scheduler):
-    def __init__(self, budget, pages, mp, thr=0, seqs=256, swap=False, host=0):
-        super().__init__(budget, pages, mp, max_num_seqs=seqs, long_prefill_token_threshold=thr,
-                         preempt_swap=swap, num_host_pages=host)
-        self._cfg = (budget, mp * P, thr, seqs, pages)
+    def __init__(self, budget, pages, mp, thr=0, seqs=256, swap=False, host=0, page_size=P):
+        super().__init__(budget, pages, mp, page_size=page_size, max_num_seqs=seqs,
+                         long_prefill_token_threshold=thr, preempt_swap=swap,
+                         num_host_pages=host)
+        self._cfg = (budget, mp * page_size, thr, seqs, pages)
+        self._page = page_size
 
 
 @pytest.mark.parametrize("swap", [False, True])
@@ -202,3 +205,23 @@ def test_request_validation():
         s.add_request(2, 5, 1)  # duplicate live id
     with pytest.raises(mcp.MCPError):
         s.add_request(3, 0, 1)
+
+
+@pytest.mark.parametrize("page_size", [1, 8, 64])
+@pytest.mark.parametrize("swap", [False, True])
+def test_random_traffic_other_page_sizes(page_size, swap):
+    """The same traffic with 1-, 8- and 64-token pages (the pool holds the
+    same number of tokens): page-aligned block tables, no page shared, every
+    request finishes and every page comes back."""
+    rng = np.random.Generator(np.random.PCG64(40 + swap))
+    pages, mp, host = 60 * P // page_size, 40 * P // page_size, 200 * P // page_size
+    s = Sched(256, pages, mp, thr=96, seqs=12, swap=swap, host=host, page_size=page_size)
+    reqs = {}
+    for rid in range(25):
+        pl, mn, pr = int(rng.integers(1, 300)), int(rng.integers(1, 40)), int(rng.integers(0, 3))
+        reqs[rid] = (pl, mn, pr)
+        s.add_request(rid, pl, mn, pr)
+    done, _ = run_random_traffic(s, reqs, 3000)
+    assert done == set(reqs), f"unfinished: {set(reqs) - done}"
+    st = s.stats()
+    assert st["free_pages"] == pages and st["finished"] == 25
