@@ -223,7 +223,9 @@ def check_plan_covers(w, items, comb, plan):
             assert it["num_heads"] == HG and it["kv_head"] % HG == 0
         else:
             assert it["q_count"] * G <= 128 and it["kv_begin"] % 128 == 0
-            assert it["q_count"] * G > 16 or lq * G > 16
+            # small segments take tiles only where the decode path is not built
+            decode_built = w.head_dim <= 128 and w.page_size >= 8
+            assert it["q_count"] * G > 16 or lq * G > 16 or not decode_built
             assert it["num_heads"] == 1
         for j in range(int(it["num_heads"])):
             h = int(it["kv_head"]) + j
@@ -274,6 +276,21 @@ def test_planner_covers_every_row_once(name):
     st, plan, items, comb = plan_host(desc_for(w), cu, w.k_lens)
     assert st == 0
     check_plan_covers(w, items, comb, plan)
+
+
+@pytest.mark.parametrize("name", ["tiny", "worked", "balanced"])
+@pytest.mark.parametrize("head_dim,page_size", [(256, None), (None, 1), (96, 8)])
+def test_planner_covers_every_row_once_other_shapes(name, head_dim, page_size):
+    """head_dim 256 and 1-token pages put decodes on tensor-core tiles;
+    every (token, kv head) row is still covered exactly once."""
+    w = synth.make_workload(name, head_dim=head_dim, page_size=page_size)
+    cu, _, _, _ = oracle.segment_layout(w.q_lens, w.k_lens)
+    for dsplit, psplit in [(0, 0), (16, 128)]:
+        st, plan, items, comb = plan_host(desc_for(w), cu, w.k_lens, dsplit=dsplit, psplit=psplit)
+        assert st == 0
+        check_plan_covers(w, items, comb, plan)
+        if w.head_dim == 256 or w.page_size == 1:
+            assert plan.num_decode_items == 0
 
 
 @pytest.mark.parametrize("dsplit,psplit", [(16, 128), (48, 256), (1024, 1024)])
