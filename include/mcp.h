@@ -25,8 +25,11 @@
  * --------------------------------
  *  - Every tensor is caller-owned.  Device tensors are dense, row-major,
  *    16-byte aligned; bf16 is IEEE bfloat16 stored as 2 bytes.
- *  - The library allocates no device memory.  Calls that need scratch take a
- *    caller-provided device workspace sized by mcp_mixed_attn_plan().
+ *  - The library allocates no device memory at run time.  Calls that need
+ *    scratch take a caller-provided device workspace sized by
+ *    mcp_mixed_attn_plan().  The one exception is mcp_mixed_attn_fwd_noalloc,
+ *    whose scratch is a fixed 16 MiB device array that the library holds on
+ *    every GPU it is loaded on, for as long as the process runs.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Device work is enqueued asynchronously on it; host-only calls ignore it.
  *  - Return value: MCP_OK, or an mcp_status error.  Argument errors are found on
@@ -77,6 +80,12 @@ const char* mcp_last_error(void);
 /* MCP_ABI_VERSION of the loaded library. */
 int32_t mcp_abi_version(void);
 
+/* How the loaded library was built: MCP_BUILD_CHECKED when it was compiled
+ * with MCP_CHECKED defined (a debugging build whose mcp_paged_kv_append also
+ * checks on the device that its slots are distinct), else 0. */
+#define MCP_BUILD_CHECKED 0x1
+int32_t mcp_build_flags(void);
+
 /* ------------------------------------------------------------------------- */
 /* a1: paged KV append                                                       */
 /* ------------------------------------------------------------------------- */
@@ -88,7 +97,11 @@ int32_t mcp_abi_version(void);
  * through slot_mapping, then run attention" step of [W] "输入组装" and [L] 4.2
  * (physical address translation, scattered writes).  Slots must be distinct
  * within one call (the result is then independent of thread order; [L] 4.2's
- * atomics are not needed).  Slots >= num_pages * P are not written and are
+ * atomics are not needed); a slot mapping with a repeated slot gives an
+ * undefined cache row, except in MCP_CHECKED builds (mcp_build_flags()), where
+ * a second kernel compares every pair of slots and sets MCP_DEVERR_SLOT_DUP
+ * (O(num_tokens^2) work: a debugging aid).  mcp_build_slot_mapping never
+ * produces one.  Slots >= num_pages * P are not written and are
  * reported by mcp_check_device_errors() as MCP_ERR_DEVICE_CHECK.
  *
  * k_new, v_new  device, bf16 [num_tokens, num_kv_heads, head_dim]
@@ -110,8 +123,9 @@ mcp_status mcp_paged_kv_append(const void* k_new, const void* v_new, const int64
  * position pos = seqlens_k[s] - Lq_s + (t - cu_seqlens_q[s]) and gets
  *   slot = block_tables[s][pos / P] * P + pos % P.
  * All pointers are HOST memory.  slot_mapping receives cu_seqlens_q[S] values.
- * Returns MCP_ERR_INVALID_ARG on malformed metadata or a page id outside
- * [0, num_pages).
+ * Returns MCP_ERR_INVALID_ARG on malformed metadata, a page id outside
+ * [0, num_pages), or two new tokens that land in the same slot (a physical page
+ * listed twice in the block tables); slot_mapping is then partly written.
  */
 mcp_status mcp_build_slot_mapping(const int32_t* block_tables, int32_t num_seqs,
                                   int32_t max_pages_per_seq, int32_t page_size, int32_t num_pages,
@@ -138,7 +152,13 @@ typedef struct mcp_plan_options {
   int32_t num_sms;              /* 0 = query the current device                  */
   int32_t decode_split_tokens;  /* KV tokens per decode work item; 0 = auto      */
   int32_t prefill_split_tokens; /* KV tokens per prefill work item; 0 = auto     */
-  int32_t reserved[5];          /* must be 0                                     */
+  int32_t test_stall;           /* 0 in production.  1 (for failure-detection    */
+                                /* tests): every tensor-core item leaves its Q   */
+                                /* tile unloaded and every device wait gives up  */
+                                /* after ~1 ms, so those items end through the   */
+                                /* bounded-wait abort path: no output rows, the  */
+                                /* error word reports MCP_ERR_TIMEOUT            */
+  int32_t reserved[4];          /* must be 0                                     */
 } mcp_plan_options;
 
 /* Filled by mcp_mixed_attn_plan(); read by mcp_mixed_attn_fwd().  Plain data:
@@ -157,7 +177,8 @@ typedef struct mcp_plan {
   int64_t workspace_bytes;    /* bytes the workspace must have                   */
   mcp_attn_desc desc;         /* the description the plan was built for          */
   int32_t combine_rows;       /* query rows (token, head) merged by the combine  */
-  int32_t reserved[7];
+  int32_t test_stall;         /* mcp_plan_options.test_stall                     */
+  int32_t reserved[6];
 } mcp_plan;
 
 /*
@@ -288,6 +309,8 @@ mcp_status mcp_merge_states(const float* o_parts, const float* lse_parts, int32_
  *  - a step whose plan needs more than 16 MiB of scratch returns
  *    MCP_ERR_WORKSPACE_TOO_SMALL before anything is launched;
  *  - every GPU that loads the library holds the 16 MiB array until exit;
+ *  - argument errors (bad metadata, NULL or misaligned tensors) are returned
+ *    before the array is touched or anything is enqueued;
  *  - all calls share that array (it keeps the last call's contents; this call
  *    clears what must start at zero), so calls whose GPU work overlaps -- on
  *    different streams or from different threads -- race; order them;
@@ -565,6 +588,7 @@ mcp_status mcp_mixed_attn_fwd_varlen(const mcp_plan* plan, const void* q, const 
 #define MCP_DEVERR_SLOT_RANGE 0x4   /* an append slot outside the pool           */
 #define MCP_DEVERR_ROW_RANGE 0x8    /* a gathered row index outside the source   */
 #define MCP_DEVERR_ITEM_KIND 0x10   /* a work item this head_dim has no path for */
+#define MCP_DEVERR_SLOT_DUP 0x20    /* two append tokens share a slot (MCP_CHECKED) */
 
 #ifdef __cplusplus
 }

@@ -15,7 +15,10 @@ import numpy as np
 
 from . import _capi
 from ._capi import (  # noqa: F401
+    DEVERR_ITEM_KIND,
     DEVERR_PAGE_RANGE,
+    DEVERR_ROW_RANGE,
+    DEVERR_SLOT_DUP,
     DEVERR_SLOT_RANGE,
     DEVERR_TIMEOUT,
     AttnDesc,

@@ -20,6 +20,10 @@ MCP_ERR_DEVICE_CHECK = 6
 DEVERR_TIMEOUT = 0x1
 DEVERR_PAGE_RANGE = 0x2
 DEVERR_SLOT_RANGE = 0x4
+DEVERR_ROW_RANGE = 0x8
+DEVERR_ITEM_KIND = 0x10
+DEVERR_SLOT_DUP = 0x20
+BUILD_CHECKED = 0x1
 
 
 class AttnDesc(ctypes.Structure):
@@ -41,7 +45,8 @@ class PlanOptions(ctypes.Structure):
         ("num_sms", c_int32),
         ("decode_split_tokens", c_int32),
         ("prefill_split_tokens", c_int32),
-        ("reserved", c_int32 * 5),
+        ("test_stall", c_int32),
+        ("reserved", c_int32 * 4),
     ]
 
 
@@ -64,7 +69,8 @@ class Plan(ctypes.Structure):
         ("workspace_bytes", c_int64),
         ("desc", AttnDesc),
         ("combine_rows", c_int32),
-        ("reserved", c_int32 * 7),
+        ("test_stall", c_int32),
+        ("reserved", c_int32 * 6),
     ]
 
 
@@ -122,6 +128,7 @@ SIGNATURES = {
     "mcp_status_string": (c_char_p, [c_int32]),
     "mcp_last_error": (c_char_p, []),
     "mcp_abi_version": (c_int32, []),
+    "mcp_build_flags": (c_int32, []),
     "mcp_paged_kv_append": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
                                       c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
     "mcp_build_slot_mapping": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p,
@@ -179,11 +186,8 @@ SIGNATURES = {
 _lib = None
 
 
-def load(path: str = LIB_PATH):
-    """Load the CUDA library; raise if it was not built (there is no fallback)."""
-    global _lib
-    if _lib is not None:
-        return _lib
+def open_library(path: str):
+    """A ctypes handle on the library at ``path`` with every signature set."""
     if not os.path.exists(path):
         raise RuntimeError(
             f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
@@ -193,8 +197,16 @@ def load(path: str = LIB_PATH):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
     return lib
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library; raise if it was not built (there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    _lib = open_library(path)
+    return _lib
 
 
 class MCPError(RuntimeError):

@@ -89,6 +89,38 @@ __global__ void __launch_bounds__(256) copy_pages_kernel(
   }
 }
 
+#ifdef MCP_CHECKED
+// Checked builds only: flag two tokens of one append that share a slot.  Each
+// block stages a 1024-slot window of the mapping in shared memory and every
+// token of the grid-stride loop compares its slot with the window's later
+// tokens; the blocks cover all windows.  O(T^2) compares: a debugging aid.
+__global__ void __launch_bounds__(256) slot_dup_check_kernel(const int64_t* __restrict__ slots,
+                                                             int32_t num_tokens, int32_t* err) {
+  constexpr int kWin = 1024;
+  __shared__ int64_t win[kWin];
+  const int32_t nwin = (num_tokens + kWin - 1) / kWin;
+  for (int32_t wi = blockIdx.x; wi < nwin; wi += gridDim.x) {
+    const int32_t w0 = wi * kWin;
+    const int32_t wn = num_tokens - w0 < kWin ? num_tokens - w0 : kWin;
+    __syncthreads();
+    for (int32_t i = threadIdx.x; i < wn; i += blockDim.x) win[i] = slots[w0 + i];
+    __syncthreads();
+    // tokens t < w0 + wn against window tokens u > t
+    const int32_t tend = w0 + wn;
+    for (int32_t t = threadIdx.x; t < tend; t += blockDim.x) {
+      const int64_t s = slots[t];
+      if (s < 0) continue;
+      const int32_t u0 = t + 1 > w0 ? t + 1 - w0 : 0;
+      for (int32_t u = u0; u < wn; ++u)
+        if (win[u] == s) {
+          if (err) atomicOr(err, MCP_DEVERR_SLOT_DUP);
+          break;
+        }
+    }
+  }
+}
+#endif
+
 int grid_for(int64_t total) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -136,6 +168,13 @@ int launch_append(const void* k_new, const void* v_new, const int64_t* slot_mapp
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, total,
       vec_per_tok, num_slots, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
       error_word);
+#ifdef MCP_CHECKED
+  if (num_tokens > 1) {
+    const int32_t nwin = (num_tokens + 1023) / 1024;
+    slot_dup_check_kernel<<<nwin, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        slot_mapping, num_tokens, error_word);
+  }
+#endif
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -59,6 +59,7 @@ namespace mcp {
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per wait
+constexpr uint64_t kTestWaitLimitNs = 1000ull * 1000ull;       // 1 ms (test_stall plans)
 constexpr float kRescaleThreshold = 8.0f;  // rescale O only when the max grows by > 2^8
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
@@ -120,17 +121,18 @@ struct Ctx {
   uint32_t bar;
   volatile int* abort;
   int32_t* err;
+  uint64_t limit_ns;  // bound of every wait: kWaitLimitNs, or kTestWaitLimitNs
   __device__ __forceinline__ uint32_t b(int i) const { return bar + 8u * static_cast<uint32_t>(i); }
 };
 
 __device__ __noinline__ bool wait_slow(volatile int* abort, int32_t* err, uint32_t bar,
-                                       uint32_t parity) {
+                                       uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = ptx::globaltimer_ns();
 #pragma unroll 1
   while (true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (ptx::globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       if (err) atomicOr(err, MCP_DEVERR_TIMEOUT);
       return false;
@@ -139,10 +141,10 @@ __device__ __noinline__ bool wait_slow(volatile int* abort, int32_t* err, uint32
 }
 
 // Wait for the phase with `parity` of barrier `bar` to complete; false if the
-// CTA aborted or the wait ran past kWaitLimitNs (then the CTA aborts).
+// CTA aborted or the wait ran past c.limit_ns (then the CTA aborts).
 __device__ __forceinline__ bool wait_on(const Ctx& c, uint32_t bar, uint32_t parity) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
-  return wait_slow(c.abort, c.err, bar, parity);
+  return wait_slow(c.abort, c.err, bar, parity, c.limit_ns);
 }
 
 // wait_on for a warp that goes on to .sync.aligned tcgen05 instructions: every
@@ -154,17 +156,20 @@ __device__ __forceinline__ bool wait_on_warp(const Ctx& c, uint32_t bar, uint32_
 
 // Bounded wait that ignores the abort flag: used to let this CTA's own async
 // copies / MMAs finish before it exits.
-__device__ __noinline__ void drain_wait(volatile int* abort, int32_t* err, uint32_t bar,
-                                        uint32_t parity) {
+__device__ __noinline__ void drain_wait_slow(volatile int* abort, int32_t* err, uint32_t bar,
+                                             uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = ptx::globaltimer_ns();
 #pragma unroll 1
   while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (ptx::globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       if (err) atomicOr(err, MCP_DEVERR_TIMEOUT);
       return;
     }
   }
+}
+__device__ __forceinline__ void drain_wait(const Ctx& c, uint32_t bar, uint32_t parity) {
+  drain_wait_slow(c.abort, c.err, bar, parity, c.limit_ns);
 }
 
 struct KParams {
@@ -194,6 +199,8 @@ struct KParams {
   const __nv_bfloat16* vc;
   const int32_t* cu_k; // non-paged K/V: first row of each segment's keys (else nullptr)
   float scale_log2;    // sm_scale * log2(e): scores live in log2 units
+  int32_t test_stall;  // testing only: 1 = tensor-core items never issue their Q-tile load,
+                       // so their softmax waits run out (1 ms bound) and the CTA aborts
 };
 
 struct Seg {
@@ -256,7 +263,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
   constexpr uint32_t kIdPV = ptx::idesc_bf16(128, D, true);
   if (warp == 0) {
     // ---------------------------------------- Q tile (TMA), then P V issuer
-    if (lane == 0) {
+    if (lane == 0 && !p.test_stall) {
       ptx::mbar_arrive_expect_tx(c.b(BQ), C::kHalves * G * TQ * 128);
       for (int h = 0; h < C::kHalves; ++h)
         ptx::tma_load_3d(sQ + h * C::kQPanel, tm_q, c.b(BQ), 64 * h, it.kv_head * G,
@@ -313,8 +320,8 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     }
     if (lane == 0) ptx::mma_commit(c.b(BDRAIN));  // arrives once this warp's MMAs are done
     __syncwarp();
-    drain_wait(c.abort, c.err, c.b(BDRAIN), 0);
-    drain_wait(c.abort, c.err, c.b(BQ), 0);
+    drain_wait(c, c.b(BDRAIN), 0);
+    if (!p.test_stall) drain_wait(c, c.b(BQ), 0);  // the Q tile's copy (none was issued)
   } else if (warp >= 6 && p.gather) {
     // ------------------- K/V producers for 1-token pages: cp.async gathers
     // Every key is its own page, so a TMA box would carry one 128-byte row;
@@ -453,7 +460,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     // drain: the last tile this warp issued into each stage
     for (int s = 0; s < NS && s < t; ++s) {
       const int last = s + ((t - 1 - s) / NS) * NS;
-      drain_wait(c.abort, c.err, c.b(full0 + s), (last / NS) & 1);
+      drain_wait(c, c.b(full0 + s), (last / NS) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ Q K^T issuer
@@ -487,7 +494,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     }
     if (lane == 0) ptx::mma_commit(c.b(BDRAIN));
     __syncwarp();
-    drain_wait(c.abort, c.err, c.b(BDRAIN), 0);
+    drain_wait(c, c.b(BDRAIN), 0);
   } else {
     // ------------------------------------------- softmax + epilogue (2-5)
     const int qw = warp & 3;
@@ -727,7 +734,7 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
     }
     for (int s = 0; s < NS && s < issued; ++s) {
       const int last = s + ((issued - 1 - s) / NS) * NS;
-      drain_wait(c.abort, c.err, c.b(BFULL0 + s), (last / NS) & 1);
+      drain_wait(c, c.b(BFULL0 + s), (last / NS) & 1);
     }
     return;
   }
@@ -1004,6 +1011,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + C::kOffBar + kNumBars * 8);
   c.abort = reinterpret_cast<volatile int*>(gb + C::kOffBar + kNumBars * 8 + 16);
   c.err = p.err;
+  c.limit_ns = p.test_stall ? kTestWaitLimitNs : kWaitLimitNs;
   const bool prefill = it.kind == kPrefillItem;
 
   if (threadIdx.x == 0) {
@@ -1199,6 +1207,7 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   kp.G = G;
   kp.dec_stages = decode_stages<D>(HG);
   kp.scale_log2 = a.sm_scale * kLog2e;
+  kp.test_stall = a.test_stall;
   cudaError_t e = cudaFuncSetAttribute(mixed_attn_fwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return static_cast<int>(e);

@@ -74,9 +74,9 @@ extern "C" mcp_status mcp_mixed_attn_fwd_noalloc(
     const int32_t* block_tables, const int32_t* cu_seqlens_q, const int32_t* seqlens_k,
     void* out, float* lse, int32_t** error_word, void* stream) {
   try {
+    // Plan once, into host memory (the plan and its work lists together).
     mcp_plan plan;
-    mcp_status st = mcp_mixed_attn_plan_host(desc, h_cu_seqlens_q, h_seqlens_k, opts, &plan,
-                                             nullptr, 0);
+    mcp_status st = mcp::plan_to_host(desc, h_cu_seqlens_q, h_seqlens_k, opts, &plan, g_lists);
     if (st != MCP_OK) return st;
     if (plan.workspace_bytes > static_cast<int64_t>(kScratchBytes)) {
       char msg[200];
@@ -86,6 +86,11 @@ extern "C" mcp_status mcp_mixed_attn_fwd_noalloc(
                static_cast<long long>(plan.workspace_bytes), kScratchBytes);
       return fail_with(MCP_ERR_WORKSPACE_TOO_SMALL, msg);
     }
+    // Every argument error is found here, before the shared scratch is touched
+    // or anything is enqueued.
+    st = mcp::check_fwd_args(&plan, q, k_cache, v_cache, block_tables, cu_seqlens_q, seqlens_k,
+                             out, lse);
+    if (st != MCP_OK) return st;
     void* scratch = nullptr;
     cudaError_t e = scratch_address(&scratch);
     if (e != cudaSuccess) {
@@ -93,10 +98,6 @@ extern "C" mcp_status mcp_mixed_attn_fwd_noalloc(
       snprintf(msg, sizeof(msg), "scratch address lookup: %s", cudaGetErrorString(e));
       return fail_with(MCP_ERR_CUDA, msg);
     }
-    g_lists.resize(static_cast<size_t>(plan.off_part_o > 0 ? plan.off_part_o : 1));
-    st = mcp_mixed_attn_plan_host(desc, h_cu_seqlens_q, h_seqlens_k, opts, &plan, g_lists.data(),
-                                  g_lists.size());
-    if (st != MCP_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (plan.off_part_o > 0)
       e = cudaMemcpyAsync(scratch, g_lists.data(), static_cast<size_t>(plan.off_part_o),

@@ -467,6 +467,14 @@ const char* mcp_last_error(void) { return g_err; }
 
 int32_t mcp_abi_version(void) { return MCP_ABI_VERSION; }
 
+int32_t mcp_build_flags(void) {
+#ifdef MCP_CHECKED
+  return MCP_BUILD_CHECKED;
+#else
+  return 0;
+#endif
+}
+
 mcp_status mcp_paged_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
                                int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
                                int32_t page_size, int32_t num_pages, void* k_cache, void* v_cache,
@@ -518,6 +526,19 @@ mcp_status mcp_build_slot_mapping(const int32_t* block_tables, int32_t num_seqs,
       slot_mapping[t] = static_cast<int64_t>(page) * page_size + pos % page_size;
     }
   }
+  // [L] 4.2 writes through atomics; here slots are unique within a call (the
+  // append uses plain stores), so two tokens mapped to one slot -- a physical
+  // page shared by two block-table rows, or repeated in one -- are rejected.
+  const int32_t T = cu_seqlens_q[num_seqs];
+  if (T > 1) {
+    std::vector<int64_t> sorted(slot_mapping, slot_mapping + T);
+    std::sort(sorted.begin(), sorted.end());
+    const auto dup = std::adjacent_find(sorted.begin(), sorted.end());
+    if (dup != sorted.end())
+      return fail(MCP_ERR_INVALID_ARG,
+                  "slot %lld is the slot of two new tokens (a physical page appears twice in "
+                  "the block tables)", static_cast<long long>(*dup));
+  }
   return okay();
 }
 
@@ -534,10 +555,12 @@ mcp_status plan_common(const mcp_attn_desc* desc, const int32_t* cu, const int32
   if (st != MCP_OK) return st;
   if (!plan) return fail(MCP_ERR_INVALID_ARG, "plan is NULL");
   if (opts) {
-    for (int i = 0; i < 5; ++i)
+    for (int i = 0; i < 4; ++i)
       if (opts->reserved[i] != 0) return fail(MCP_ERR_INVALID_ARG, "opts->reserved must be 0");
     if (opts->num_sms < 0 || opts->decode_split_tokens < 0 || opts->prefill_split_tokens < 0)
       return fail(MCP_ERR_INVALID_ARG, "negative plan option");
+    if (opts->test_stall != 0 && opts->test_stall != 1)
+      return fail(MCP_ERR_INVALID_ARG, "opts->test_stall must be 0 or 1");
   }
   st = validate_meta(desc->num_seqs, desc->total_q, desc->page_size, desc->max_pages_per_seq, cu, sk);
   if (st != MCP_OK) return st;
@@ -586,6 +609,7 @@ mcp_status plan_common(const mcp_attn_desc* desc, const int32_t* cu, const int32
   pl.off_error = align256(pl.off_part_lse + b.part_rows * 4);
   pl.workspace_bytes = pl.off_error + 256;
   pl.desc = *desc;
+  pl.test_stall = opts ? opts->test_stall : 0;
   *plan = pl;
   return MCP_OK;
 }
@@ -598,6 +622,41 @@ void write_lists(const mcp_plan& pl, const Built& b, unsigned char* dst) {
 }
 
 }  // namespace
+
+namespace mcp {
+
+mcp_status check_fwd_args(const mcp_plan* plan, const void* q, const void* k_cache,
+                          const void* v_cache, const int32_t* block_tables,
+                          const int32_t* cu_seqlens_q, const int32_t* seqlens_k, const void* out,
+                          const float* lse) {
+  if (!plan || plan->magic != kPlanMagic) return fail(MCP_ERR_INVALID_ARG, "plan not initialised");
+  if (plan->num_items == 0) return MCP_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !cu_seqlens_q || !seqlens_k || !out)
+    return fail(MCP_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return fail(MCP_ERR_INVALID_ARG, "q / caches / out must be 16-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(MCP_ERR_INVALID_ARG, "lse not 4-byte aligned");
+  return MCP_OK;
+}
+
+mcp_status plan_to_host(const mcp_attn_desc* desc, const int32_t* h_cu_seqlens_q,
+                        const int32_t* h_seqlens_k, const mcp_plan_options* opts, mcp_plan* plan,
+                        std::vector<unsigned char>& lists) {
+  try {
+    Built b;
+    mcp_status st = plan_common(desc, h_cu_seqlens_q, h_seqlens_k, opts, plan, b);
+    if (st != MCP_OK) return st;
+    lists.resize(static_cast<size_t>(std::max<int64_t>(1, plan->off_part_o)));
+    write_lists(*plan, b, lists.data());
+    return MCP_OK;
+  } catch (const std::bad_alloc&) {
+    return fail(MCP_ERR_INVALID_ARG, "host allocation failed while planning");
+  } catch (...) {
+    return fail(MCP_ERR_INVALID_ARG, "unexpected host error while planning");
+  }
+}
+
+}  // namespace mcp
 
 extern "C" {
 
@@ -773,15 +832,13 @@ mcp_status mcp_mixed_attn_fwd(const mcp_plan* plan, const void* q, const void* k
                               const void* v_cache, const int32_t* block_tables,
                               const int32_t* cu_seqlens_q, const int32_t* seqlens_k, void* out,
                               float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!plan || plan->magic != kPlanMagic) return fail(MCP_ERR_INVALID_ARG, "plan not initialised");
+  mcp_status st = mcp::check_fwd_args(plan, q, k_cache, v_cache, block_tables, cu_seqlens_q,
+                                      seqlens_k, out, lse);
+  if (st != MCP_OK) return st;
   const mcp_attn_desc& d = plan->desc;
   if (plan->num_items == 0) return okay();
-  if (!q || !k_cache || !v_cache || !block_tables || !cu_seqlens_q || !seqlens_k || !out || !workspace)
-    return fail(MCP_ERR_INVALID_ARG, "NULL pointer argument");
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
-    return fail(MCP_ERR_INVALID_ARG, "q / caches / out must be 16-byte aligned");
+  if (!workspace) return fail(MCP_ERR_INVALID_ARG, "NULL pointer argument (workspace)");
   if (!aligned(workspace, 256)) return fail(MCP_ERR_INVALID_ARG, "workspace not 256-byte aligned");
-  if (lse && !aligned(lse, 4)) return fail(MCP_ERR_INVALID_ARG, "lse not 4-byte aligned");
   if (static_cast<int64_t>(workspace_bytes) < plan->workspace_bytes)
     return fail(MCP_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %lld needed", workspace_bytes,
                 static_cast<long long>(plan->workspace_bytes));
@@ -811,6 +868,7 @@ mcp_status mcp_mixed_attn_fwd(const mcp_plan* plan, const void* q, const void* k
   a.max_pages_per_seq = d.max_pages_per_seq;
   a.num_pages = d.num_pages;
   a.sm_scale = d.sm_scale;
+  a.test_stall = plan->test_stall;
   int e = mcp::launch_mixed_attn(a, stream);
   if (e != 0) return cuda_fail(e, "mixed_attn_fwd launch");
   e = mcp::launch_combine(a, stream);
@@ -867,6 +925,7 @@ mcp_status mcp_mixed_attn_fwd_varlen(const mcp_plan* plan, const void* q, const 
   a.max_pages_per_seq = d.max_pages_per_seq;
   a.num_pages = d.num_pages;
   a.sm_scale = d.sm_scale;
+  a.test_stall = plan->test_stall;
   int e = mcp::launch_mixed_attn(a, stream);
   if (e != 0) return cuda_fail(e, "mixed_attn_fwd launch");
   e = mcp::launch_combine(a, stream);

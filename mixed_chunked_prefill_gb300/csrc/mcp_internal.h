@@ -5,6 +5,10 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <vector>
+
+#include "mcp.h"
+
 namespace mcp {
 
 enum ItemKind : int32_t { kDecodeItem = 0, kPrefillItem = 1 };
@@ -83,6 +87,7 @@ struct FwdArgs {
   // keys are rows cu_seqlens_k[s] .. cu_seqlens_k[s+1]-1; block tables unused
   const int32_t* cu_seqlens_k = nullptr;
   int64_t total_k = 0;
+  int32_t test_stall = 0;  // mcp_plan_options.test_stall of the plan
 };
 
 // Launchers (return a cudaError_t value; 0 = success).  Defined in *.cu.
@@ -106,5 +111,20 @@ int32_t set_error_code(int32_t status, const char* msg);
 // Message of the last launcher failure that was not a CUDA error (e.g. a tensor
 // map the driver rejected), "" otherwise.
 const char* launch_detail();
+
+// Host-side checks of mcp_mixed_attn_fwd's arguments other than the
+// workspace: the plan, non-NULL tensors and their alignment.  MCP_OK when the
+// plan has no work item.  Defined in host.cpp.
+mcp_status check_fwd_args(const mcp_plan* plan, const void* q, const void* k_cache,
+                          const void* v_cache, const int32_t* block_tables,
+                          const int32_t* cu_seqlens_q, const int32_t* seqlens_k, const void* out,
+                          const float* lse);
+
+// mcp_mixed_attn_plan_host in one pass: fills *plan and resizes `lists` to the
+// first plan->off_part_o bytes of the workspace layout (at least one byte),
+// holding the work items and combine entries.  Defined in host.cpp.
+mcp_status plan_to_host(const mcp_attn_desc* desc, const int32_t* h_cu_seqlens_q,
+                        const int32_t* h_seqlens_k, const mcp_plan_options* opts, mcp_plan* plan,
+                        std::vector<unsigned char>& lists);
 
 }  // namespace mcp

@@ -70,31 +70,35 @@ def per_segment_rel_rms(w, out, ref_out):
     return res
 
 
-def sub_workload(w, t, segs):
-    """The segments ``segs`` of ``w`` as their own workload (same lengths, same
-    physical pages), with their slices of the tensors on the CPU -- so the oracle
-    can check a few rows of a workload too large to run whole."""
-    import torch
+class SegmentKV:
+    """The keys and values of each segment in position order, taken straight
+    from the generated inputs: history positions 0 .. H_s - 1 (``k_hist``
+    slice of segment s) followed by this step's tokens (its ``k_new`` rows,
+    the last Lq_s positions; [W] "输入组装").
 
-    cu = np.concatenate([[0], np.cumsum(w.q_lens)])
-    hcu = np.concatenate([[0], np.cumsum(w.hist_lens)])
-    sub = synth.Workload(w.name + "-sub", w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
-                         w.sm_scale, [w.q_lens[s] for s in segs], [w.k_lens[s] for s in segs],
-                         w.seed)
-    bt_full = w.block_tables()
-    sub.page_perm = w.page_perm
-    rows_bt = np.full((len(segs), sub.max_pages_per_seq), -1, dtype=np.int32)
-    for i, s in enumerate(segs):
-        n = w.pages_of(s)
-        rows_bt[i, :n] = bt_full[s, :n]
-    sub.block_tables = lambda: rows_bt  # same physical pages as in the full workload
-    ts = {}
-    for name in ("q", "k_new", "v_new"):
-        ts[name] = torch.cat([t[name][cu[s]:cu[s + 1]] for s in segs]).cpu()
-    for name in ("k_hist", "v_hist"):
-        ts[name] = torch.cat([t[name][hcu[s]:hcu[s + 1]] for s in segs]).cpu()
-    return sub, ts
+    It stands in for the oracle's dict page store (same ``gather`` call) on
+    the full-size workloads, whose tens of GB of history are too large to
+    hold as per-slot dict entries; the GPU's page translation is then checked
+    against no page table at all.  Each segment is copied to the host and
+    widened to float64 only while the oracle works on it."""
+
+    def __init__(self, w, t):
+        self.t = t
+        self.cu = np.concatenate([[0], np.cumsum(w.q_lens)]).astype(np.int64)
+        self.hcu = np.concatenate([[0], np.cumsum(w.hist_lens)]).astype(np.int64)
+
+    def gather(self, table, s, length):
+        import torch
+
+        h0, h1 = int(self.hcu[s]), int(self.hcu[s + 1])
+        q0, q1 = int(self.cu[s]), int(self.cu[s + 1])
+        assert (h1 - h0) + (q1 - q0) == length
+        out = []
+        for hist, new in (("k_hist", "k_new"), ("v_hist", "v_new")):
+            rows = torch.cat([self.t[hist][h0:h1], self.t[new][q0:q1]]).cpu()
+            out.append(oracle.bf16_bits_to_f64(synth.bf16_bits(rows)))
+        return out[0], out[1]
 
 
-__all__ = ["gpu_step", "compare", "per_segment_rel_rms", "sub_workload", "OracleStep", "oracle",
+__all__ = ["SegmentKV", "gpu_step", "compare", "per_segment_rel_rms", "OracleStep", "oracle",
            "ATOL", "RMS_TOL", "LSE_TOL"]

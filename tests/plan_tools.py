@@ -21,12 +21,14 @@ def desc_for(w):
                          w.page_size, w.max_pages_per_seq, w.num_pages, w.sm_scale)
 
 
-def plan_host(desc, cu, sk, num_sms=152, dsplit=0, psplit=0):
-    """(status, plan, items, combine) from mcp_mixed_attn_plan_host."""
+def plan_host(desc, cu, sk, num_sms=152, dsplit=0, psplit=0, opts=None):
+    """(status, plan, items, combine) from mcp_mixed_attn_plan_host (``opts``
+    replaces num_sms / dsplit / psplit when given)."""
     lib = mcp.load()
     cu = np.ascontiguousarray(np.asarray(cu, dtype=np.int32))
     sk = np.ascontiguousarray(np.asarray(sk, dtype=np.int32))
-    opts = mcp.PlanOptions(num_sms, dsplit, psplit)
+    if opts is None:
+        opts = mcp.PlanOptions(num_sms, dsplit, psplit)
     plan = mcp.Plan()
     st = lib.mcp_mixed_attn_plan_host(ctypes.byref(desc), cu.ctypes.data_as(ctypes.c_void_p),
                                       sk.ctypes.data_as(ctypes.c_void_p), ctypes.byref(opts),

@@ -118,6 +118,21 @@ def test_plan_rejects_null_and_reserved_options():
                                         ctypes.byref(plan), None, 0) == _capi.MCP_ERR_INVALID_ARG
 
 
+def test_plan_records_test_stall_and_rejects_other_values():
+    """test_stall (failure-detection tests only) is 0 or 1 and travels in the
+    plan to the forward call; it changes no work item."""
+    opts = mcp.PlanOptions(152, 0, 0)
+    st0, plan0, items0, _ = plan_host(base_desc(), CU, SK, opts=opts)
+    opts.test_stall = 1
+    st1, plan1, items1, _ = plan_host(base_desc(), CU, SK, opts=opts)
+    assert st0 == st1 == 0
+    assert plan0.test_stall == 0 and plan1.test_stall == 1
+    assert np.array_equal(items0, items1)
+    opts.test_stall = 2
+    st2, *_ = plan_host(base_desc(), CU, SK, opts=opts)
+    assert st2 == _capi.MCP_ERR_INVALID_ARG
+
+
 def test_plan_host_buffer_too_small():
     lib = mcp.load()
     st, plan, _, _ = plan_host(base_desc(), CU, SK)
@@ -192,6 +207,38 @@ def test_slot_mapping_rejects_page_outside_pool():
     bt = np.array([[0, 1, 99]], dtype=np.int32)
     with pytest.raises(mcp.MCPError):
         mcp.build_slot_mapping(bt, [0, 3], [40], 16, 10)
+
+
+def test_slot_mapping_rejects_shared_slots():
+    """[L] 4.2 writes through atomics; the append here relies on distinct slots
+    instead, so a step whose new tokens share a slot is refused on the host."""
+    # two decodes whose last page is the same physical page 4, at the same offset
+    bt = np.array([[0, 4], [1, 4]], dtype=np.int32)
+    with pytest.raises(mcp.MCPError) as ei:
+        mcp.build_slot_mapping(bt, [0, 1, 2], [20, 20], 16, 10)
+    assert ei.value.status == _capi.MCP_ERR_INVALID_ARG
+    assert b"two new tokens" in mcp.load().mcp_last_error()
+    # the same page at different offsets is not a shared slot
+    got = mcp.build_slot_mapping(bt, [0, 1, 2], [20, 21], 16, 10)
+    assert got.tolist() == [4 * 16 + 3, 4 * 16 + 4]
+    # a page repeated inside one row, both positions written this step
+    bt1 = np.array([[3, 3]], dtype=np.int32)
+    with pytest.raises(mcp.MCPError):
+        mcp.build_slot_mapping(bt1, [0, 32], [32], 16, 10)
+
+
+def test_checked_build_exports_the_same_abi_and_says_so():
+    """The MCP_CHECKED variant (device-side duplicate-slot check in the append)
+    builds, exports every declared symbol and reports its build flag; the
+    default library does not."""
+    from mixed_chunked_prefill_gb300 import build
+
+    path = build.build(checked=True)
+    lib = _capi.open_library(path)
+    for n in header_functions():
+        assert hasattr(lib, n), n
+    assert lib.mcp_build_flags() == _capi.BUILD_CHECKED
+    assert mcp.load().mcp_build_flags() == 0
 
 
 # ---------------------------------------------------------------------------

@@ -36,3 +36,30 @@ def test_describe_names_the_overrides():
     assert synth.describe("worked") == synth.DESCRIPTIONS["worked"]
     text = synth.describe("worked", 256, 8)
     assert text.startswith(synth.DESCRIPTIONS["worked"]) and "head_dim 256" in text and "page 8" in text
+
+
+def test_segment_kv_gathers_what_the_page_store_holds():
+    """The full-size parity test reads each segment's keys through SegmentKV
+    (position order straight from the inputs); on a workload the dict page
+    store can hold, both give the same K/V, and the oracle's output over
+    either is identical."""
+    import numpy as np
+
+    import oracle
+    from gpu_harness import SegmentKV
+    from harness import OracleStep
+
+    w = synth.make_workload("balanced").shuffled(3)
+    t = w.tensors("cpu")
+    ref = OracleStep(w, t)
+    ref.do_append()
+    skv = SegmentKV(w, t)
+    for s in range(w.num_seqs):
+        K0, V0 = ref.store.gather(ref.table, s, w.k_lens[s])
+        K1, V1 = skv.gather(None, s, w.k_lens[s])
+        assert np.array_equal(K0, K1) and np.array_equal(V0, V1)
+    toks = [0, 5, 29, 30, w.total_q - 1]
+    a = ref.attention(tokens=toks)
+    b = oracle.mixed_attention(ref.q, skv, None, ref.cu_q, w.k_lens, w.num_kv_heads, w.sm_scale,
+                               tokens=toks)
+    assert np.array_equal(a[0][toks], b[0][toks]) and np.array_equal(a[1][toks], b[1][toks])
