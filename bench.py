@@ -5,8 +5,10 @@ attention forward + split combine) on synthetic inputs resident in HBM.
 
 Prints ONE JSON line (rank 0).  ``value`` is query tokens per second over the
 timed steps (all ranks), ``ms_per_step`` the device time of one step.  The
-default workload is the worked A/B/C layout (cu_seqlens_q = [0, 1, 2, 1810],
-seqlens_k = [121, 46, 10000], 32 q / 8 kv heads, head_dim 128, 16-token pages).
+default workload is the long-context step, the largest that fits one GPU: one
+2048-token chunk after 126976 history tokens plus 64 decodes over contexts
+U[65536, 131072], 32 q / 8 kv heads, head_dim 128, 16-token pages (~26 GB of
+KV read per step).
 ``--impl reference`` times the CPU oracle on a bounded sample instead.
 Under torchrun every rank runs an independent replica (the step does not
 shard); timing is the max over ranks.
@@ -319,9 +321,11 @@ def run_gpu(args, rank, world, local_rank):
         v_h = v_new.cpu().pin_memory()
         # two output buffers: consecutive steps are in flight together
         outs_h = [torch.empty_like(q_h).pin_memory() for _ in range(2)]
+        # the arenas hold this step's plan: its split partials and work lists
         hs = HostStep(w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size, w.num_pages,
                       w.sm_scale, w.total_q, w.num_seqs, w.max_pages_per_seq, device=dev,
-                      stream=stream)
+                      stream=stream, workspace_bytes=max(64 << 20, int(step.plan.workspace_bytes)),
+                      list_bytes=max(4 << 20, int(step.plan.off_part_o)))
         for i in range(3):
             hs(q_h, k_h, v_h, cu, w.k_lens, bt, k_cache, v_cache, outs_h[i & 1])
         stream.synchronize()
@@ -392,44 +396,66 @@ def run_gpu(args, rank, world, local_rank):
 # the CPU oracle (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
 
-def oracle_cores():
+def blas_threads():
+    """Threads of the BLAS NumPy's matmul runs on (threadpoolctl), or None."""
     try:
         import threadpoolctl
 
-        info = threadpoolctl.threadpool_info()
-        n = max((i.get("num_threads", 1) for i in info), default=1)
-        return int(n)
+        info = [i for i in threadpoolctl.threadpool_info() if i.get("user_api") == "blas"]
+        return int(max(i.get("num_threads", 1) for i in info)) if info else None
     except Exception:
-        return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        return None
+
+
+def oracle_cores():
+    """Host threads the oracle uses: its BLAS thread count, else the affinity size."""
+    n = blas_threads()
+    if n:
+        return n
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def host_details():
+    """What the oracle's timing ran on: core counts, architecture, BLAS threads."""
+    return {"os_cpu_count": os.cpu_count(),
+            "affinity": (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                         else None),
+            "machine": os.uname().machine, "blas_threads": blas_threads(),
+            "threading": "multi-thread: NumPy's BLAS on all its threads for the matmuls; "
+                         "masking, exp and the page gather single-threaded; no "
+                         "single-thread run was timed"}
 
 
 class OracleSample:
-    """The oracle on one workload's inputs, restricted to a row sample."""
+    """The oracle on one workload's inputs, restricted to a row sample.
+
+    The two big workloads (tens of GB of KV history) are sampled by segment:
+    the shortest and the longest decode plus the chunk, as a workload of
+    their own whose values are drawn for those segments alone (same lengths,
+    heads, page size and value distribution), so the host never holds the
+    whole history."""
 
     def __init__(self, name, head_dim=None, page_size=None):
         sys.path.insert(0, os.path.join(ROOT, "tests"))
-        import torch
-
         from harness import OracleStep
 
         w = synth.make_workload(name, head_dim=head_dim, page_size=page_size)
         self.w = w
         if name in ("decode-heavy", "long-context"):
-            # too large to hold whole: keep the chunk and two decodes
-            from gpu_harness import sub_workload
-
-            t = w.tensors("cpu")
-            dec = [s for s in range(w.num_seqs) if w.q_lens[s] == 1][:2]
+            dec = [s for s in range(w.num_seqs) if w.q_lens[s] == 1]
             chunk = [s for s in range(w.num_seqs) if w.q_lens[s] > 1]
-            w, t = sub_workload(w, t, dec + chunk)
+            segs = [min(dec, key=lambda s: w.k_lens[s]), max(dec, key=lambda s: w.k_lens[s])]
+            segs += chunk
+            w = synth.make_workload_from_lengths(
+                w.name + "-sample", w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
+                w.sm_scale, [w.q_lens[s] for s in segs], [w.k_lens[s] for s in segs], w.seed)
             self.w = w
-            self.note = "two decodes + the chunk segment of the workload"
+            self.note = ("the shortest and the longest decode + the chunk segment of the "
+                         "workload, values drawn for those segments alone")
         else:
-            t = w.tensors("cpu")
             self.note = "all segments"
-        self.step = OracleStep(w, t)
+        self.step = OracleStep(w, w.tensors("cpu"))
         self.step.do_append()
-        del torch
 
     def rows(self, n):
         """n query tokens spread over the whole stream (decodes first)."""
@@ -584,7 +610,7 @@ def cpu_baseline(name, budget_s=15.0, head_dim=None, page_size=None):
         dt = s.time_rows(rows)
     return {"value": len(rows) / dt, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",
             "sample": f"{len(rows)} of {s.w.total_q} query tokens (all heads), {s.note}; "
-                      f"{dt:.1f} s", "seconds": dt}
+                      f"{dt:.1f} s", "seconds": dt, "host": host_details()}
 
 
 def run_reference(args):
@@ -611,7 +637,7 @@ def run_reference(args):
             "config": {"workload": synth.describe(args.config, args.head_dim, args.page_size),
                        "name": args.config},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_cores(),
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "host": host_details()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -621,7 +647,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="worked", choices=synth.CONFIG_NAMES + synth.PROFILE_NAMES)
+    ap.add_argument("--config", default="long-context", choices=synth.CONFIG_NAMES + synth.PROFILE_NAMES)
     ap.add_argument("--head-dim", type=int, default=None, choices=[64, 96, 128, 256],
                     help="run the workload's segments at this head_dim")
     ap.add_argument("--page-size", type=int, default=None, choices=[1, 8, 16, 32, 64],
