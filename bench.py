@@ -383,12 +383,18 @@ def run_gpu(args, rank, world, local_rank):
                             float(np.percentile(step_ms, 90) * 1e3)],
         "kv_gbps": alg["kv_bytes"] / (ms_per_step / 1e3) / 1e9,
         "step_roofline_frac": step_roof_s / (ms_per_step / 1e3),
+        "step_roofline_us": step_roof_s * 1e6,
         "plan_host_us": plan_us,
         "roofline": roof,
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
     }
+    if step_roof_s < 2e-6:
+        # a step whose bytes and FLOPs take under 2 us at the peaks is bound by launch
+        # latency and per-item set-up, not by HBM or the tensor cores
+        res["launch_bound"] = (f"roofline time {step_roof_s * 1e6:.2f} us: the step is bound by "
+                               "launch latency and per-item set-up; reported, no % target")
     return res
 
 
@@ -397,14 +403,20 @@ def run_gpu(args, rank, world, local_rank):
 # ---------------------------------------------------------------------------
 
 def blas_threads():
-    """Threads of the BLAS NumPy's matmul runs on (threadpoolctl), or None."""
+    """Threads of the BLAS NumPy's matmul runs on (threadpoolctl), else the
+    thread count the usual environment variables set, else None."""
     try:
         import threadpoolctl
 
         info = [i for i in threadpoolctl.threadpool_info() if i.get("user_api") == "blas"]
-        return int(max(i.get("num_threads", 1) for i in info)) if info else None
+        if info:
+            return int(max(i.get("num_threads", 1) for i in info))
     except Exception:
-        return None
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return None
 
 
 def oracle_cores():
@@ -420,7 +432,9 @@ def host_details():
     return {"os_cpu_count": os.cpu_count(),
             "affinity": (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
                          else None),
-            "machine": os.uname().machine, "blas_threads": blas_threads(),
+            "machine": os.uname().machine,
+            "blas_threads": blas_threads() or "not reported (no threadpoolctl; OpenBLAS "
+                                              "defaults to every core of the affinity set)",
             "threading": "multi-thread: NumPy's BLAS on all its threads for the matmuls; "
                          "masking, exp and the page gather single-threaded; no "
                          "single-thread run was timed"}
