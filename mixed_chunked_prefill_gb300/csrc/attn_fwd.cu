@@ -669,6 +669,279 @@ __device__ __forceinline__ uint32_t keep_pair(uint32_t v, int k, int nvalid) {
   return v & (lo | hi);
 }
 
+// The last step of a decode item whose head is shared by several warps: warp
+// (hw, po = 0) merges the warps' (m, l, O) states of head hw, left in shared
+// memory as mo [8 warps][16 rows][D], mm and ml [8 warps][16 rows], and writes
+// the rows (lane -> row lane % 16, columns half lane / 16).
+template <int D>
+__device__ __forceinline__ void merge_rows(const KParams& p, const WorkItem& it, const Seg& sg,
+                                           const float* mo, const float* mm, const float* ml,
+                                           int hw, int HG, int ps, int head, int R, int lane) {
+  const int G = p.G;
+  const bool direct = it.part_row < 0;
+  const int r = lane & 15;
+  if (r >= R) return;
+  const int d0 = (lane >> 4) * (D / 2);
+  float M = neg_inf();
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (k < ps) M = fmaxf(M, mm[(hw + k * HG) * 16 + r]);
+  float wt[8], L = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    wt[k] = 0.f;
+    if (k < ps) {
+      const float mk = mm[(hw + k * HG) * 16 + r];
+      wt[k] = mk == neg_inf() ? 0.f : ptx::ex2(mk - M);
+      L += wt[k] * ml[(hw + k * HG) * 16 + r];
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int tok = it.q_begin + r / G;
+  const int g = r - (r / G) * G;
+  const size_t orow = static_cast<size_t>(sg.q_start + tok) * p.hq + head * G + g;
+  for (int d = 0; d < D / 2 && d0 + d < p.dr; d += 4) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k >= ps) break;
+      const float4 v = *reinterpret_cast<const float4*>(mo + ((hw + k * HG) * 16 + r) * D + d0 + d);
+      a[0] += wt[k] * v.x;
+      a[1] += wt[k] * v.y;
+      a[2] += wt[k] * v.z;
+      a[3] += wt[k] * v.w;
+    }
+    if (direct) {
+      uint2 pk2 = make_uint2(ptx::pack_bf16x2(a[0] * inv, a[1] * inv), ptx::pack_bf16x2(a[2] * inv, a[3] * inv));
+      *reinterpret_cast<uint2*>(p.out + orow * p.dr + d0 + d) = pk2;
+    } else {
+      *reinterpret_cast<float4*>(p.part_o + static_cast<size_t>(it.part_row + hw * it.part_head_stride + r) * p.dr + d0 + d) =
+          make_float4(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv);
+    }
+  }
+  if (lane < 16) {
+    const float lse = L > 0.f ? (M + log2f(L)) * kLn2 : neg_inf();
+    if (direct) {
+      if (p.lse) p.lse[orow] = lse;
+    } else {
+      p.part_lse[it.part_row + hw * it.part_head_stride + r] = lse;
+    }
+  }
+}
+
+
+// Decode consumer for at most 8 query rows of a kv head (G * Lq <= 8: every
+// plain decode with G <= 8).  The scores are taken transposed, S^T = K Q^T,
+// with m16n8k16: 16 keys fill M and the query rows N = 8, so one MMA covers
+// 16 keys per 16 dims (rows in M would leave 8 of 16 rows empty at G = 8 and
+// 12 at G = 4).  Likewise O^T = V^T P^T: 16 dims in M, the rows in N.  The
+// MMA count per page is half the row-major form's, and so are the
+// accumulator and Q registers.  P^T, the B operand of the second product, is
+// moved from the score layout (lane holds keys gid, gid + 8 of rows 2 tig,
+// 2 tig + 1) to the B layout (lane holds row gid, keys 2 tig, +1, +8, +9)
+// with four shuffles.
+template <int D>
+__device__ __forceinline__ void decode_n8(const Ctx& c, const WorkItem& it, const Seg& sg,
+                                          const KParams& p, uint8_t* gb, uint32_t ring, int NS,
+                                          int stage_bytes, int block, int box_bytes, int npg,
+                                          int HG, int hw, int ps, int po, int cw, int lane) {
+  const int G = p.G;
+  const int B = 1 << p.box_log2;
+  const int kv0 = it.kv_begin, kv1 = it.kv_end;
+  const int head = it.kv_head + hw;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int R = it.q_count * G;
+  const int last_tok = it.q_count - 1;
+  const float sl2 = p.scale_log2;
+  // rows of the C fragments: 2 tig and 2 tig + 1; their last visible key
+  int jm[2];
+  bool rv[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int r = 2 * tig + e;
+    rv[e] = r < R;
+    const int tk = r / G < last_tok ? r / G : last_tok;
+    jm[e] = min(sg.hist + it.q_begin + tk, kv1 - 1);
+  }
+  // Q^T as B fragments: lane holds row gid, dims 16 kk + 2 tig (+1) and + 8 (+9)
+  uint32_t qb[D / 16][2];
+  {
+    const bool vr = gid < R;
+    const uint32_t* qr = reinterpret_cast<const uint32_t*>(
+        p.q + (static_cast<size_t>(sg.q_start + it.q_begin + (vr ? gid / G : 0)) * p.hq + head * G +
+               (vr ? gid % G : 0)) * p.dr);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const bool in = vr && kk * 16 < p.dr;  // columns past the tensors' head_dim are 0
+      qb[kk][0] = in ? qr[kk * 8 + tig] : 0u;
+      qb[kk][1] = in ? qr[kk * 8 + 4 + tig] : 0u;
+    }
+  }
+  float o[D / 16][4];  // O^T: dims 16 mt + gid (+8) x rows 2 tig (+1)
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m[2] = {neg_inf(), neg_inf()}, l[2] = {0.f, 0.f};
+  bool ok = true;
+  const int mi = lane >> 3, rr = lane & 7;
+  const int hstr = p.panel_boxes ? B * 128 : Cfg<D>::kHalves * B * 128;  // between heads
+  const uint32_t pstr = static_cast<uint32_t>(p.panel_boxes ? HG * B * 128 : B * 128);  // panels
+  auto row_off = [&](int tk) -> uint32_t {
+    return static_cast<uint32_t>((tk >> p.box_log2) * box_bytes + hw * hstr + (tk & (B - 1)) * 128);
+  };
+  // ldmatrix rows: K as A (keys x dims): matrices (keys 0-7, c) (8-15, c) (0-7, c+1) (8-15, c+1);
+  // V^T as A via .trans of V (keys x dims): (keys 0-7, c) (0-7, c+1) (8-15, c) (8-15, c+1)
+  const uint32_t offK = row_off((mi & 1) * 8 + rr);
+  const int chK = mi >> 1;
+  const uint32_t offV = row_off((mi >> 1) * 8 + rr);
+  const int chV = mi & 1;
+  // P^T gather sources: keys 2 tig and 2 tig + 1 of row gid
+  const int srcA = 4 * (2 * tig) + (gid >> 1), srcB = 4 * (2 * tig + 1) + (gid >> 1);
+  const bool odd_row = gid & 1;
+  for (int pi = po; pi < npg; pi += ps) {
+    const int s = pi % NS;
+    if (!(ok = wait_on(c, c.b(BFULL0 + s), (pi / NS) & 1))) break;
+    const uint32_t kb = ring + s * stage_bytes;
+    const uint32_t vb = kb + block;
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int h = kk >> 2, c0 = (kk & 3) * 2;
+      uint32_t a[4];
+      ptx::ldsm_x4(kb + offK + h * pstr + (((c0 + chK) ^ rr) << 4), a[0], a[1], a[2], a[3]);
+      ptx::mma16816((kk & 1) ? sb : sa, a, qb[kk][0], qb[kk][1]);
+    }
+    const int key0 = kv0 + pi * kPageSize;
+    // x[e]: keys gid (e = 0, 1) and gid + 8 (e = 2, 3), rows 2 tig + (e & 1)
+    float x[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int key = key0 + gid + (e >> 1) * 8;
+      x[e] = rv[e & 1] && key <= jm[e & 1] ? (sa[e] + sb[e]) * sl2 : neg_inf();
+    }
+    float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 4));
+      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 8));
+      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 16));
+    }
+    float u[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float nm = fmaxf(m[e], mx[e]);
+      if (nm > m[e] + kRescaleThreshold) {
+        const float a = ptx::ex2(m[e] - nm);
+        m[e] = nm;
+        l[e] *= a;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) { o[i][e] *= a; o[i][2 + e] *= a; }
+      }
+      u[e] = m[e] == neg_inf() ? 0.f : m[e];
+    }
+    float pv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pv[e] = ptx::ex2(x[e] - u[e & 1]);
+    l[0] += pv[0] + pv[2];
+    l[1] += pv[1] + pv[3];
+    // P^T to the B layout: row gid, keys 2 tig (+1) in b0 and 2 tig + 8 (+9) in b1
+    const uint32_t pe = ptx::pack_bf16x2(pv[0], pv[2]);  // row 2 tig:     keys gid, gid + 8
+    const uint32_t po_ = ptx::pack_bf16x2(pv[1], pv[3]); // row 2 tig + 1: keys gid, gid + 8
+    const uint32_t ae = __shfl_sync(0xffffffffu, pe, srcA), ao = __shfl_sync(0xffffffffu, po_, srcA);
+    const uint32_t be = __shfl_sync(0xffffffffu, pe, srcB), bo = __shfl_sync(0xffffffffu, po_, srcB);
+    const uint32_t va = odd_row ? ao : ae;  // keys 2 tig, 2 tig + 8 of row gid
+    const uint32_t vb2 = odd_row ? bo : be; // keys 2 tig + 1, 2 tig + 9
+    const uint32_t b0 = (va & 0xFFFFu) | (vb2 << 16);
+    const uint32_t b1 = (va >> 16) | (vb2 & 0xFFFF0000u);
+    const int nvalid = kv1 - key0;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      const int h = mt >> 2, c0 = (mt & 3) * 2;
+      uint32_t a[4];
+      ptx::ldsm_x4_t(vb + offV + h * pstr + (((c0 + chV) ^ rr) << 4), a[0], a[1], a[2], a[3]);
+      if (nvalid < kPageSize) {
+        // keys past the item's end: unused slots may hold NaN; P is 0 there
+        a[0] = keep_pair(a[0], tig * 2, nvalid);
+        a[1] = keep_pair(a[1], tig * 2, nvalid);
+        a[2] = keep_pair(a[2], 8 + tig * 2, nvalid);
+        a[3] = keep_pair(a[3], 8 + tig * 2, nvalid);
+      }
+      ptx::mma16816(o[mt], a, b0, b1);
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(c.b(BEMPTY0 + s));
+  }
+  // full row sums over the eight lanes of each row (gid)
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    l[e] += __shfl_xor_sync(0xffffffffu, l[e], 4);
+    l[e] += __shfl_xor_sync(0xffffffffu, l[e], 8);
+    l[e] += __shfl_xor_sync(0xffffffffu, l[e], 16);
+  }
+  const bool direct = it.part_row < 0;
+  if (ps == 1) {
+    // this warp alone saw its head's whole KV range: write from the fragments
+    if (!ok || *c.abort) return;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 2 * tig + e;
+      if (r >= R) continue;
+      const int tok = it.q_begin + r / G;
+      const int g = r - (r / G) * G;
+      const float inv = l[e] > 0.f ? 1.f / l[e] : 0.f;
+      const size_t orow = static_cast<size_t>(sg.q_start + tok) * p.hq + head * G + g;
+      if (direct) {
+        __nv_bfloat16* dst = p.out + orow * p.dr;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int d0 = mt * 16 + gid;
+          if (d0 < p.dr) dst[d0] = __float2bfloat16_rn(o[mt][e] * inv);
+          if (d0 + 8 < p.dr) dst[d0 + 8] = __float2bfloat16_rn(o[mt][2 + e] * inv);
+        }
+      } else {
+        float* dst = p.part_o + static_cast<size_t>(it.part_row + hw * it.part_head_stride + r) * p.dr;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int d0 = mt * 16 + gid;
+          if (d0 < p.dr) dst[d0] = o[mt][e] * inv;
+          if (d0 + 8 < p.dr) dst[d0 + 8] = o[mt][2 + e] * inv;
+        }
+      }
+      if (gid == 0) {
+        const float lse = l[e] > 0.f ? (m[e] + log2f(l[e])) * kLn2 : neg_inf();
+        if (direct) {
+          if (p.lse) p.lse[orow] = lse;
+        } else {
+          p.part_lse[it.part_row + hw * it.part_head_stride + r] = lse;
+        }
+      }
+    }
+    return;
+  }
+  // several warps per head: merge their (m, l, O) through shared memory, in the
+  // layout of the 16-row consumer ([warp][16 rows][D]; rows 8-15 unused)
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  float* mo = reinterpret_cast<float*>(gb);
+  float* mm = mo + 8 * 16 * D;
+  float* ml = mm + 8 * 16;
+  float* mine = mo + cw * 16 * D;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int r = 2 * tig + e;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      mine[r * D + mt * 16 + gid] = o[mt][e];
+      mine[r * D + mt * 16 + gid + 8] = o[mt][2 + e];
+    }
+    if (gid == 0) {
+      mm[cw * 16 + r] = m[e];
+      ml[cw * 16 + r] = l[e];
+    }
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  if (po != 0 || !ok || *c.abort) return;
+  merge_rows<D>(p, it, sg, mo, mm, ml, hw, HG, ps, head, R, lane);
+}
+
 template <int D>
 __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, const Seg& sg,
                                             const KParams& p, uint32_t base, uint8_t* gb,
@@ -745,6 +1018,11 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
   const int hw = cw % HG;        // kv head (within the group) of this warp
   const int ps = 8 / HG;         // warps sharing that head
   const int po = cw / HG;        // this warp takes pages po, po + ps, ...
+  if (it.q_count * G <= 8) {
+    decode_n8<D>(c, it, sg, p, gb, ring, NS, stage_bytes, block, box_bytes, npg, HG, hw, ps, po, cw,
+                 lane);
+    return;
+  }
   const int head = it.kv_head + hw;
   const int gid = lane >> 2, tig = lane & 3;
   const int R = it.q_count * G;
@@ -941,55 +1219,7 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
   }
   asm volatile("bar.sync 1, 256;" ::: "memory");
   if (po != 0 || !ok || *c.abort) return;
-  // warp (hw, po = 0) finishes head hw: lane -> row lane % 16, columns half (lane / 16)
-  const int r = lane & 15;
-  if (r >= R) return;
-  const int d0 = (lane >> 4) * (D / 2);
-  float M = neg_inf();
-#pragma unroll
-  for (int k = 0; k < 8; ++k)
-    if (k < ps) M = fmaxf(M, mm[(hw + k * HG) * 16 + r]);
-  float wt[8], L = 0.f;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    wt[k] = 0.f;
-    if (k < ps) {
-      const float mk = mm[(hw + k * HG) * 16 + r];
-      wt[k] = mk == neg_inf() ? 0.f : ptx::ex2(mk - M);
-      L += wt[k] * ml[(hw + k * HG) * 16 + r];
-    }
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const int tok = it.q_begin + r / G;
-  const int g = r - (r / G) * G;
-  const size_t orow = static_cast<size_t>(sg.q_start + tok) * p.hq + head * G + g;
-  for (int d = 0; d < D / 2 && d0 + d < p.dr; d += 4) {
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k >= ps) break;
-      const float4 v = *reinterpret_cast<const float4*>(mo + ((hw + k * HG) * 16 + r) * D + d0 + d);
-      a[0] += wt[k] * v.x;
-      a[1] += wt[k] * v.y;
-      a[2] += wt[k] * v.z;
-      a[3] += wt[k] * v.w;
-    }
-    if (direct) {
-      uint2 pk2 = make_uint2(ptx::pack_bf16x2(a[0] * inv, a[1] * inv), ptx::pack_bf16x2(a[2] * inv, a[3] * inv));
-      *reinterpret_cast<uint2*>(p.out + orow * p.dr + d0 + d) = pk2;
-    } else {
-      *reinterpret_cast<float4*>(p.part_o + static_cast<size_t>(it.part_row + hw * it.part_head_stride + r) * p.dr + d0 + d) =
-          make_float4(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv);
-    }
-  }
-  if (lane < 16) {
-    const float lse = L > 0.f ? (M + log2f(L)) * kLn2 : neg_inf();
-    if (direct) {
-      if (p.lse) p.lse[orow] = lse;
-    } else {
-      p.part_lse[it.part_row + hw * it.part_head_stride + r] = lse;
-    }
-  }
+  merge_rows<D>(p, it, sg, mo, mm, ml, hw, HG, ps, head, R, lane);
 }
 
 template <int D>

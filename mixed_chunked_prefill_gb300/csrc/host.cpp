@@ -176,6 +176,8 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
            int32_t num_rows = 0) {
   const int G = d.num_q_heads / d.num_kv_heads;
   const int H = d.num_kv_heads;
+  // head_dim of the kernel that runs the step (96 runs the 128 one): the cost model's D
+  const int DK = d.head_dim == 96 ? 128 : d.head_dim;
   const int HG = mcp::decode_head_group(H);
   const int dopt = o ? o->decode_split_tokens : 0;
   const int popt = o ? o->prefill_split_tokens : 0;
@@ -233,10 +235,10 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
   // overlap on different SMs, which this model does not capture (measured:
   // it chose a split 2.5% slower on the long-context step).
   if (popt <= 0) {
-    const double tile_ns = 750.0 * d.head_dim / 128.0, item_ns = 5000.0;
+    const double tile_ns = 750.0 * DK / 128.0, item_ns = 5000.0;
     double pre_ns = 0.0, dec_ns = 0.0;
     for (const Unit& x : units) {
-      if (x.decode) dec_ns += vis_of(x) * 4.0 * d.head_dim * H / 45.0;
+      if (x.decode) dec_ns += vis_of(x) * 4.0 * DK * H / 45.0;
       else pre_ns += H * (item_ns + cdiv(vis_of(x), mcp::kKvTile) * tile_ns);
     }
     if (pre_ns > 0.0 && dec_ns < 0.1 * (pre_ns + dec_ns)) {
@@ -264,7 +266,7 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
             for (int64_t k = 0; k < n; ++k)
               for (int h0 = 0; h0 < H; h0 += HG)
                 cost.push_back(3000.0 + std::min<int64_t>(sz, vis_of(x) - k * sz) * 4.0 *
-                                            d.head_dim * HG / 45.0);
+                                            DK * HG / 45.0);
           } else {
             even_split(vis_of(x), cand_ps, mcp::kKvTile, &n, &sz);
             for (int64_t k = 0; k < n; ++k) {
@@ -345,7 +347,7 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
           it.kv_end = static_cast<int32_t>(std::min(vis, (k + 1) * sz));
           it.part_row = static_cast<int32_t>(n > 1 ? base + k * rows_n : -1);
           it.part_head_stride = static_cast<int32_t>(n * rows_n);
-          dec.push_back({it, (it.kv_end - it.kv_begin) * 4.0 * d.head_dim * HG / 45.0, 0});
+          dec.push_back({it, (it.kv_end - it.kv_begin) * 4.0 * DK * HG / 45.0, 0});
         }
       }
     } else {
@@ -374,7 +376,7 @@ void build(const mcp_attn_desc& d, const int32_t* cu, const int32_t* sk, int num
           const double tiles = static_cast<double>(cdiv(it.kv_end - it.kv_begin, mcp::kKvTile));
           // tiles reading the same K/V (same segment, kv head, split) share a group
           const int64_t gid = (static_cast<int64_t>(s) * H + h) * 4096 + k;
-          pre.push_back({it, 300.0 + tiles * 4.0 * 128 * 128 * d.head_dim / 6000.0, gid});
+          pre.push_back({it, 300.0 + tiles * 4.0 * 128 * 128 * DK / 6000.0, gid});
         }
       }
     }
