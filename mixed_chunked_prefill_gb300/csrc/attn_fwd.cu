@@ -962,7 +962,14 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
   const int ups = kPageSize >> p.box_log2;    // boxes per stage: 1 or 2
   const int box_bytes = block / ups;
 
-  if (warp == 0) {
+  // Two producer warps: warp 0 loads the K half of every stage, warp 1 the V
+  // half (each arrives on the stage's barrier with its bytes).  One warp
+  // issues its TMA boxes one after another, and a single producer capped one
+  // CTA's stream near 100 GB/s.
+  if (warp < 2) {
+    const bool isV = warp == 1;
+    const CUtensorMap* tm = isV ? tm_vd : tm_kd;
+    const uint32_t half_off = isV ? static_cast<uint32_t>(block) : 0u;
     const uint64_t pol = ptx::policy_evict_first();  // each page is read once
     int issued = 0;
     bool ok = true;
@@ -980,24 +987,18 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
         const int pga = __shfl_sync(0xffffffffu, pg, i * ups);
         const int pgb = __shfl_sync(0xffffffffu, pg, i * ups + ups - 1);
         if (lane == 0) {
-          const uint32_t dst = ring + s * stage_bytes;
-          ptx::mbar_arrive_expect_tx(c.b(BFULL0 + s), stage_bytes);
+          const uint32_t dst = ring + s * stage_bytes + half_off;
+          ptx::mbar_arrive_expect_tx(c.b(BFULL0 + s), block);
           for (int j = 0; j < ups; ++j) {
             const int pgi = j ? pgb : pga;
             const int tok = blk_tok(p, pgi), pgp = blk_page(p, pgi);
             if (!p.panel_boxes) {  // [head][panel][B tokens][128 B]
-              ptx::tma_load_5d(dst + j * box_bytes, tm_kd, c.b(BFULL0 + s), 0, tok, 0, it.kv_head,
-                               pgp, pol);
-              ptx::tma_load_5d(dst + block + j * box_bytes, tm_vd, c.b(BFULL0 + s), 0, tok, 0,
-                               it.kv_head, pgp, pol);
+              ptx::tma_load_5d(dst + j * box_bytes, tm, c.b(BFULL0 + s), 0, tok, 0, it.kv_head, pgp,
+                               pol);
             } else {  // one box per panel: [panel][head][B tokens][128 B]
-              for (int h = 0; h < C::kHalves; ++h) {
-                const int off = j * box_bytes + h * HG * B * 128;
-                ptx::tma_load_4d(dst + off, tm_kd, c.b(BFULL0 + s), 64 * h, tok, it.kv_head, pgp,
-                                 pol);
-                ptx::tma_load_4d(dst + block + off, tm_vd, c.b(BFULL0 + s), 64 * h, tok,
-                                 it.kv_head, pgp, pol);
-              }
+              for (int h = 0; h < C::kHalves; ++h)
+                ptx::tma_load_4d(dst + j * box_bytes + h * HG * B * 128, tm, c.b(BFULL0 + s),
+                                 64 * h, tok, it.kv_head, pgp, pol);
             }
           }
         }
@@ -1011,7 +1012,6 @@ __device__ __forceinline__ void decode_item(const Ctx& c, const WorkItem& it, co
     }
     return;
   }
-  if (warp < 2) return;
 
   // ---------------------------------------------------- consumers (2-9)
   const int cw = warp - 2;
@@ -1251,6 +1251,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (i == BP0 || i == BP0 + 1 || i == BQT) count = 128;  // every softmax thread
       if (i == BDRAIN) count = 2;                       // the Q K^T and the P V issuer
       if (i >= BEMPTY0) count = prefill ? 1 : it.num_heads;  // one warp per head reads a stage
+      // a decode stage: the K-half and the V-half producer warps arrive
+      if (!prefill && i >= BFULL0 && i < BFULL0 + kMaxDecStages) count = 2;
       ptx::mbar_init(c.b(i), count);
     }
     *c.abort = 0;
