@@ -204,6 +204,56 @@ def test_checked_build_flags_duplicate_slots_on_the_device():
     assert append(mcp.load(), dup) == 0  # the default build does not look
 
 
+@pytest.mark.parametrize("name,dsplit,psplit", [("tiny", 16, 128), ("worked", 16, 0),
+                                                ("balanced", 0, 0)])
+def test_outputs_and_workspace_stay_in_bounds(name, dsplit, psplit):
+    """Canary bytes before and after the output, the LSE and the workspace
+    come back bit-identical: the fused kernel and the combine write only the
+    step's rows and the plan's workspace bytes."""
+    import mixed_chunked_prefill_gb300 as mcp
+    from mixed_chunked_prefill_gb300.step import MixedStep, write_history
+
+    w = synth.make_workload(name)
+    t = w.tensors("cpu")
+    ref = OracleStep(w, t)
+    ref.do_append()
+    ref_out, ref_lse = ref.attention()
+    td = {k: v.cuda() for k, v in t.items()}
+    shape = (w.num_pages, w.page_size, w.num_kv_heads, w.head_dim)
+    kc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    write_history(w.block_tables(), w.hist_lens, td["k_hist"], td["v_hist"], kc, vc, w.page_size)
+    cu = np.concatenate([[0], np.cumsum(w.q_lens)]).astype(np.int32)
+    opts = mcp.PlanOptions(0, dsplit, psplit)
+    step = MixedStep(w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size, w.num_pages,
+                     w.sm_scale, cu, w.k_lens, w.block_tables(), options=opts)
+    step.append(td["k_new"], td["v_new"], kc, vc)
+    guard = 4096  # bytes on each side (a multiple of 256 keeps every buffer aligned)
+    sizing = mcp.mixed_attn_plan(step.desc, cu, w.k_lens, opts)
+    ws_big = torch.full((int(sizing.workspace_bytes) + 2 * guard,), 0xA5, dtype=torch.uint8,
+                        device="cuda")
+    ws = ws_big[guard:guard + int(sizing.workspace_bytes)]
+    plan = mcp.mixed_attn_plan(step.desc, cu, w.k_lens, opts, ws)
+    n_out = w.total_q * w.num_q_heads * w.head_dim
+    ge = guard // 2
+    out_big = torch.full((n_out + 2 * ge,), -7.0, dtype=torch.bfloat16, device="cuda")
+    out_big[ge:ge + n_out] = float("nan")
+    out = out_big[ge:ge + n_out].view(w.total_q, w.num_q_heads, w.head_dim)
+    gl = guard // 4
+    n_lse = w.total_q * w.num_q_heads
+    lse_big = torch.full((n_lse + 2 * gl,), -3.0, dtype=torch.float32, device="cuda")
+    lse = lse_big[gl:gl + n_lse].view(w.total_q, w.num_q_heads)
+    before_ws = ws_big.clone()
+    mcp.mixed_attn_fwd(plan, td["q"], kc, vc, step.bt_d, step.cu_d, step.sk_d, out, lse, ws)
+    mcp.check_device_errors(mcp.workspace_error_word(plan, ws))
+    torch.cuda.synchronize()
+    assert torch.equal(ws_big[:guard], before_ws[:guard])
+    assert torch.equal(ws_big[-guard:], before_ws[-guard:])
+    assert bool((out_big[:ge] == -7.0).all()) and bool((out_big[-ge:] == -7.0).all())
+    assert bool((lse_big[:gl] == -3.0).all()) and bool((lse_big[-gl:] == -3.0).all())
+    compare(w, out, lse, ref_out, ref_lse, label=f"canary/{name}")
+
+
 def test_merge_states_matches_oracle():
     import mixed_chunked_prefill_gb300 as mcp
     import oracle
