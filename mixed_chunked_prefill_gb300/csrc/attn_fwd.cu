@@ -19,13 +19,14 @@
 //    they read (S buffer t & 1) and rescale O lazily.  Only tiles that cross
 //    the diagonal are masked ([K] "掩码特化").
 //  * decode item -- the G*Lq (<= 16) query rows of each kv head of a head group
-//    (up to 8 heads) against a KV range.  Warp 0 streams 16 tokens of the
-//    group per ring stage -- one TMA box for K and one for V, laid out in
-//    shared memory as [head][panel][token][64] (two boxes each for 8-token
-//    pages) -- through a multi-stage ring; warps 2-9 each own one kv head
-//    (ldmatrix + mma.sync m16n8k16, quad-shuffle max/sum, online softmax);
-//    several warps share a head when the group is smaller than 8 and merge
-//    their states at the end.
+//    (up to 8 heads) against a KV range.  Warps 0 and 1 stream 16 tokens of
+//    the group per ring stage -- warp 0 the TMA box of K, warp 1 the box of
+//    V, laid out in shared memory as [head][panel][token][64] (two boxes each
+//    for 8-token pages) -- through a multi-stage ring; warps 2-9 each own one
+//    kv head (ldmatrix + mma.sync m16n8k16, shuffle max/sum, online softmax;
+//    with at most 8 rows the products are taken transposed, the keys in M and
+//    the rows in N, see decode_n8); several warps share a head when the group
+//    is smaller than 8 and merge their states at the end.
 //
 // head_dim 96 runs the D = 128 instantiation on 96-wide tensors: the tensor
 // maps span 96 columns, TMA fills columns 96-127 of every box with zeros, V
