@@ -343,9 +343,25 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     constexpr int kChunks = D / 8;          // 16-byte pieces of a key row
     const size_t head_off = static_cast<size_t>(it.kv_head) * p.dr;
     const size_t page_elems = static_cast<size_t>(p.hkv) * p.dr;  // one token per page
+    const int32_t* bt_row = p.bt + static_cast<size_t>(it.seg) * p.max_pages;
+    // the block-table entries (one page per key) of tile t + 1 are read while
+    // tile t's copies are issued, so the dependent load is off the copy path
+    int raw_next[kKeysPer];
+#pragma unroll
+    for (int j = 0; j < kKeysPer; ++j) {
+      const int pos = kv0 + tid + 64 * j;
+      raw_next[j] = ntiles > 0 && pos < kv1 ? bt_row[pos] : -1;
+    }
     int t = 0;
     for (; t < ntiles; ++t) {
       const int s = t % NS;
+      int raw[kKeysPer];
+#pragma unroll
+      for (int j = 0; j < kKeysPer; ++j) {
+        raw[j] = raw_next[j];
+        const int pos = kv0 + (t + 1) * kKvTile + tid + 64 * j;
+        raw_next[j] = t + 1 < ntiles && pos < kv1 ? bt_row[pos] : -1;
+      }
       if (t >= NS && !wait_on(c, c.b(empty0 + s), ((t / NS) + 1) & 1)) break;
       const uint32_t stage = isK ? sK(s) : sV(s);
 #pragma unroll
@@ -354,7 +370,7 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
         const int pos = kv0 + t * kKvTile + key;
         int page = -1;
         if (pos < kv1) {
-          const int v = p.bt[static_cast<size_t>(it.seg) * p.max_pages + pos];
+          const int v = raw[j];
           if (v >= 0 && v < p.num_pages) page = v;
           else atomicOr(p.err, MCP_DEVERR_PAGE_RANGE);
         }
