@@ -440,6 +440,14 @@ def host_details():
                          "single-thread run was timed"}
 
 
+def sample_segments(w):
+    """The segments the CPU legs time on a big workload: the shortest and the
+    longest decode plus every chunk segment."""
+    dec = [s for s in range(w.num_seqs) if w.q_lens[s] == 1]
+    chunk = [s for s in range(w.num_seqs) if w.q_lens[s] > 1]
+    return [min(dec, key=lambda s: w.k_lens[s]), max(dec, key=lambda s: w.k_lens[s])] + chunk
+
+
 class OracleSample:
     """The oracle on one workload's inputs, restricted to a row sample.
 
@@ -456,10 +464,7 @@ class OracleSample:
         w = synth.make_workload(name, head_dim=head_dim, page_size=page_size)
         self.w = w
         if name in ("decode-heavy", "long-context"):
-            dec = [s for s in range(w.num_seqs) if w.q_lens[s] == 1]
-            chunk = [s for s in range(w.num_seqs) if w.q_lens[s] > 1]
-            segs = [min(dec, key=lambda s: w.k_lens[s]), max(dec, key=lambda s: w.k_lens[s])]
-            segs += chunk
+            segs = sample_segments(w)
             w = synth.make_workload_from_lengths(
                 w.name + "-sample", w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
                 w.sm_scale, [w.q_lens[s] for s in segs], [w.k_lens[s] for s in segs], w.seed)
