@@ -555,30 +555,32 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
       const int s = t & 1;
       if (!(ok = wait_on_warp(c, c.b(BS0 + s), (t >> 1) & 1))) break;
       ptx::tc_fence_after();
+      // the scores, and the max of each 32 of them from the load itself
       uint32_t r[kKvTile];
+      float mj[kKvTile / 32];
 #pragma unroll
-      for (int j = 0; j < kKvTile / 32; ++j) ptx::tmem_ld32(tS + s * kKvTile + j * 32, r + j * 32);
+      for (int j = 0; j < kKvTile / 32; ++j) ptx::tmem_ld32_max(tS + s * kKvTile + j * 32, r + j * 32, mj[j]);
 #pragma unroll
-      for (int j = 0; j < kKvTile / 32; ++j) ptx::tmem_wait_ld_dep(r + j * 32);
+      for (int j = 0; j < kKvTile / 32; ++j) ptx::tmem_wait_ld_dep_max(r + j * 32, mj[j]);
       const int key0 = kv0 + t * kKvTile;
-      // max of the raw scores (sm_scale > 0 keeps the order), eight independent chains
-      float mxp[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) mxp[j] = neg_inf();
+      // max of the raw scores (sm_scale > 0 keeps the order)
+      float mx;
       if (key0 + kKvTile - 1 <= jmax) {  // every key of the tile is visible to this row
-#pragma unroll
-        for (int i = 0; i < kKvTile; i += 2)
-          mxp[(i >> 1) & 7] = ptx::max3(mxp[(i >> 1) & 7], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+        mx = kKvTile == 128 ? fmaxf(fmaxf(mj[0], mj[1]), fmaxf(mj[kKvTile / 32 - 2], mj[kKvTile / 32 - 1]))
+                            : fmaxf(mj[0], mj[kKvTile / 32 - 1]);
       } else {  // diagonal / last tile: mask keys past this row's last visible key
+        float mxp[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mxp[j] = neg_inf();
 #pragma unroll
         for (int i = 0; i < kKvTile; ++i) {
           const float x = (key0 + i <= jmax) ? __uint_as_float(r[i]) : neg_inf();
           r[i] = __float_as_uint(x);
           mxp[i & 7] = fmaxf(mxp[i & 7], x);
         }
+        mx = ptx::max3(ptx::max3(mxp[0], mxp[1], mxp[2]), ptx::max3(mxp[3], mxp[4], mxp[5]),
+                       fmaxf(mxp[6], mxp[7]));
       }
-      const float mx = ptx::max3(ptx::max3(mxp[0], mxp[1], mxp[2]), ptx::max3(mxp[3], mxp[4], mxp[5]),
-                                 fmaxf(mxp[6], mxp[7]));
       const float m_new = fmaxf(m_ref, mx * sl2);
       const bool rescale = m_new > m_ref + kRescaleThreshold;
       float alpha = 1.f;
