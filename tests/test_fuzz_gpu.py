@@ -3,7 +3,9 @@
 Each case draws a step the fixed tests do not spell out -- kv heads, group
 size, head_dim, page size, and a mix of decode segments, speculative
 multi-token segments, chunks with and without history, empty segments -- and
-sometimes forces split KV ranges.  Every row is compared with the oracle
+sometimes forces split KV ranges.  A second family takes large GQA groups
+(6 to 128 query heads per kv head), speculative segments of up to 16 tokens
+and histories up to 6000 keys.  Every row is compared with the oracle
 ([W] "Flash Attention 的 varlen 接口": each segment sees its own KV,
 right-aligned), the caches bit-exact after the append, unused slots NaN.
 """
@@ -70,5 +72,38 @@ def random_step(seed):
 def test_random_mixed_step(seed):
     w, o = random_step(seed)
     label = (f"fuzz{seed}: H {w.num_q_heads}/{w.num_kv_heads} D {w.head_dim} P {w.page_size} "
+             f"q {w.q_lens} k {w.k_lens} split {o is not None}")
+    full_parity(w, options=o, label=label)
+
+
+def random_wide_step(seed):
+    """(workload, plan options) of one seeded random step with a large group."""
+    rng = np.random.Generator(np.random.PCG64(50000 + seed))
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([6, 12, 16, 32, 64, 128]))
+    while hkv * g > 256:
+        g //= 2
+    d = int(rng.choice([64, 96, 128, 256]))
+    page = int(rng.choice([8, 16, 32, 64]))
+    q_lens, k_lens = [], []
+    for _ in range(int(rng.integers(1, 6))):
+        kind = rng.choice(["decode", "spec", "chunk", "fresh"])
+        hist = int(rng.integers(0, 6000))
+        lq = {"decode": 1, "spec": int(rng.integers(2, 17)), "chunk": int(rng.integers(2, 200)),
+              "fresh": int(rng.integers(1, 200))}[kind]
+        if kind == "fresh":  # a prompt's first chunk: no history
+            hist = 0
+        q_lens.append(lq)
+        k_lens.append(lq + hist)
+    w = synth.make_workload_from_lengths(f"wide{seed}", hkv * g, hkv, d, page, 1 / math.sqrt(d),
+                                         q_lens, k_lens, 900 + seed)
+    o = opts(int(rng.choice([16, 64, 512])), int(rng.choice([128, 1024]))) if rng.random() < 0.5 else None
+    return w, o
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_wide_step(seed):
+    w, o = random_wide_step(seed)
+    label = (f"wide{seed}: H {w.num_q_heads}/{w.num_kv_heads} D {w.head_dim} P {w.page_size} "
              f"q {w.q_lens} k {w.k_lens} split {o is not None}")
     full_parity(w, options=o, label=label)
