@@ -215,8 +215,10 @@ mcp_status mcp_mixed_attn_plan(const mcp_attn_desc* desc, const int32_t* h_cu_se
 /*
  * Same plan as mcp_mixed_attn_plan, written to HOST memory instead of a
  * device workspace: host_buffer receives the first plan->off_part_o bytes of
- * the workspace layout (the work items at plan->off_items and the combine
- * entries at plan->off_combine).  A caller that copies those bytes to the
+ * the workspace layout (the work items at plan->off_items, the combine
+ * entries at plan->off_combine and, right after them, the combine's index of
+ * the entry holding the first row of each block of 8 merged rows, int32).
+ * A caller that copies those bytes to the
  * start of its device workspace and zeroes the 4-byte error word at
  * plan->off_error gets the same state mcp_mixed_attn_plan uploads.
  * host_buffer == NULL: sizing only.  Host only; needs no GPU when

@@ -34,8 +34,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 // One warp per merged row.  The rows of all entries are numbered
 // consecutively (entry e owns rows [row_base, row_base + rows)), so the grid
 // covers exactly the rows that have parts, whatever the mix of short decode
-// entries and 128-row chunk tiles.  Lane k holds the LSE of part k (32 parts
-// per pass); lane l accumulates columns [l * D/32, (l + 1) * D/32) of O.
+// entries and 128-row chunk tiles.  The plan stores, right after the
+// entries, the entry of each block's first row; a warp steps forward from it
+// to its own row's entry (a block's 8 rows span at most 8 entries).  Lane k
+// holds the LSE of part k (32 parts per pass); lane l accumulates columns
+// [l * D/32, (l + 1) * D/32) of O.
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineEntry* __restrict__ ents,
                                                       int num_ents, int total_rows,
@@ -45,16 +48,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineEntry* __rest
                                                       __nv_bfloat16* __restrict__ out,
                                                       float* __restrict__ lse, int hq, int G) {
   constexpr int V = D / 32;
-  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int r = blockIdx.x * kCombineRowsPerBlock + (threadIdx.x >> 5);
   if (r >= total_rows) return;
   const int lane = threadIdx.x & 31;
   // the entry holding flat row r: the last one with row_base <= r
-  int lo = 0, hi = num_ents - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(&ents[mid].row_base) <= r) lo = mid;
-    else hi = mid - 1;
-  }
+  const int32_t* block_ent = reinterpret_cast<const int32_t*>(ents + num_ents);
+  int lo = __ldg(&block_ent[blockIdx.x]);
+  while (lo + 1 < num_ents && __ldg(&ents[lo + 1].row_base) <= r) ++lo;
   const CombineEntry e = ents[lo];
   const int row = r - e.row_base;
   const int n = e.num_splits;
@@ -148,7 +148,7 @@ int launch_combine(const FwdArgs& a, void* stream) {
   if (a.num_combine <= 0 || a.combine_rows <= 0) return 0;
   const int G = a.num_q_heads / a.num_kv_heads;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int blocks = (a.combine_rows + 7) / 8;
+  const int blocks = (a.combine_rows + kCombineRowsPerBlock - 1) / kCombineRowsPerBlock;
   if (a.head_dim == 128) {
     combine_kernel<128><<<blocks, 256, 0, st>>>(
         a.combine, a.num_combine, a.combine_rows, a.cu_seqlens_q, a.part_o, a.part_lse,

@@ -605,8 +605,12 @@ mcp_status plan_common(const mcp_attn_desc* desc, const int32_t* cu, const int32
   pl.partial_rows = b.part_rows;
   pl.off_items = 0;
   pl.off_combine = align256(static_cast<int64_t>(b.items.size()) * sizeof(mcp::WorkItem));
-  pl.off_part_o =
-      align256(pl.off_combine + static_cast<int64_t>(b.comb.size()) * sizeof(mcp::CombineEntry));
+  // after the entries: for every block of kCombineRowsPerBlock merged rows,
+  // the entry that holds its first row (the combine starts its search there)
+  const int64_t cidx = (crow + mcp::kCombineRowsPerBlock - 1) / mcp::kCombineRowsPerBlock;
+  pl.off_part_o = align256(pl.off_combine +
+                           static_cast<int64_t>(b.comb.size()) * sizeof(mcp::CombineEntry) +
+                           cidx * static_cast<int64_t>(sizeof(int32_t)));
   pl.off_part_lse = align256(pl.off_part_o + b.part_rows * desc->head_dim * 4);
   pl.off_error = align256(pl.off_part_lse + b.part_rows * 4);
   pl.workspace_bytes = pl.off_error + 256;
@@ -619,8 +623,17 @@ mcp_status plan_common(const mcp_attn_desc* desc, const int32_t* cu, const int32
 void write_lists(const mcp_plan& pl, const Built& b, unsigned char* dst) {
   std::memset(dst, 0, static_cast<size_t>(pl.off_part_o));
   if (!b.items.empty()) std::memcpy(dst, b.items.data(), b.items.size() * sizeof(mcp::WorkItem));
-  if (!b.comb.empty())
+  if (!b.comb.empty()) {
     std::memcpy(dst + pl.off_combine, b.comb.data(), b.comb.size() * sizeof(mcp::CombineEntry));
+    // block index: entry of the first row of each block of merged rows
+    int32_t* idx = reinterpret_cast<int32_t*>(dst + pl.off_combine +
+                                              b.comb.size() * sizeof(mcp::CombineEntry));
+    size_t e = 0;
+    for (int64_t r = 0; r < pl.combine_rows; r += mcp::kCombineRowsPerBlock) {
+      while (e + 1 < b.comb.size() && b.comb[e + 1].row_base <= r) ++e;
+      *idx++ = static_cast<int32_t>(e);
+    }
+  }
 }
 
 }  // namespace

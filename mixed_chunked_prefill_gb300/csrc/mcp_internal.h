@@ -57,6 +57,9 @@ struct CombineEntry {
   int32_t row_base;  // rows of all entries are numbered consecutively: this entry's first
 };
 static_assert(sizeof(CombineEntry) == 32, "CombineEntry layout");
+// merged rows per combine block (one warp each); the plan stores, after the
+// combine entries, the entry of the first row of every such block
+constexpr int kCombineRowsPerBlock = 8;
 
 struct FwdArgs {
   const void* q;
