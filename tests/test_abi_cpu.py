@@ -354,6 +354,37 @@ def test_planner_forced_splits(dsplit, psplit):
             assert plan.num_combine > 0 or name == "tiny"
 
 
+@pytest.mark.parametrize("name,dsplit,psplit", [("worked", 16, 256), ("balanced", 0, 0),
+                                                ("balanced", 64, 1024), ("tiny", 16, 128)])
+def test_combine_block_index(name, dsplit, psplit):
+    """After the combine entries the plan stores, for every block of 8 merged
+    rows, the entry that holds the block's first row; the lists region
+    (off_part_o bytes) covers it."""
+    lib = mcp.load()
+    w = synth.make_workload(name)
+    cu, _, _, _ = oracle.segment_layout(w.q_lens, w.k_lens)
+    st, plan, items, comb = plan_host(desc_for(w), cu, w.k_lens, dsplit=dsplit, psplit=psplit)
+    assert st == 0 and plan.num_combine > 0
+    cu32 = np.ascontiguousarray(np.asarray(cu, dtype=np.int32))
+    sk32 = np.ascontiguousarray(np.asarray(w.k_lens, dtype=np.int32))
+    buf = np.zeros(int(plan.off_part_o), dtype=np.uint8)
+    opts = mcp.PlanOptions(152, dsplit, psplit)
+    assert lib.mcp_mixed_attn_plan_host(ctypes.byref(desc_for(w)), cu32.ctypes.data_as(ctypes.c_void_p),
+                                        sk32.ctypes.data_as(ctypes.c_void_p), ctypes.byref(opts),
+                                        ctypes.byref(plan), buf.ctypes.data_as(ctypes.c_void_p),
+                                        buf.size) == 0
+    nblocks = -(-int(plan.combine_rows) // 8)
+    start = int(plan.off_combine) + int(plan.num_combine) * 32
+    assert start + 4 * nblocks <= int(plan.off_part_o)
+    idx = buf[start:start + 4 * nblocks].view("<i4")
+    assert int(comb["row_base"][0]) == 0
+    assert int(comb["row_base"][-1] + comb["rows"][-1]) == int(plan.combine_rows)
+    for b, e in enumerate(idx):
+        r = 8 * b
+        assert 0 <= e < plan.num_combine
+        assert comb["row_base"][e] <= r < comb["row_base"][e] + comb["rows"][e]
+
+
 def test_planner_random_shapes():
     rng = np.random.Generator(np.random.PCG64(123))
     for trial in range(40):
