@@ -200,6 +200,8 @@ struct KParams {
   const __nv_bfloat16* vc;
   const int32_t* cu_k; // non-paged K/V: first row of each segment's keys (else nullptr)
   float scale_log2;    // sm_scale * log2(e): scores live in log2 units
+  int32_t k_box5;      // 1: 8-token boxes of K carry every 64-column panel (one box per 8
+                       // keys, landing [panel][8 keys][128 B]); 0: one box per panel
   int32_t test_stall;  // testing only: 1 = tensor-core items never issue their Q-tile load,
                        // so their softmax waits run out (1 ms bound) and the CTA aborts
 };
@@ -443,7 +445,14 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
         if (lane == 0) {
           const uint32_t bar = c.b(full0 + s);
           ptx::mbar_arrive_expect_tx(bar, C::kKvBytes / 2);
-          if (isK) {
+          if (isK && B == 8 && p.k_box5) {
+            // one box per 8 keys with every panel: [box][panel][8 keys][128 B]
+            const uint32_t dst = sK(s);
+#pragma unroll
+            for (int i = 0; i < nu; ++i)
+              ptx::tma_load_5d(dst + (u0 + i) * (C::kHalves * 1024), tm, bar, 0,
+                               blk_tok(p, pgs[i]), 0, it.kv_head, blk_page(p, pgs[i]), pol);
+          } else if (isK) {
             const uint32_t dst = sK(s);
 #pragma unroll
             for (int i = 0; i < nu; ++i)
@@ -483,7 +492,13 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
     // ------------------------------------------------------ Q K^T issuer
     const uint32_t tS = tmem;              // S buffers
     const uint32_t tQ = tmem + C::kColQ;   // Q: D/2 columns, two bf16 per column
-    const uint64_t dK0 = ptx::sdesc_sw128(sK(0), 16, 1024);
+    // K tile layouts: one box per panel, [panel][128 keys][128 B] (8-key
+    // groups 1024 B apart, panels kKPanel apart); or, with 8-token boxes of
+    // every panel (p.k_box5), [box][panel][8 keys][128 B] (8-key groups one
+    // box, kHalves KB, apart; panels 1 KB apart)
+    const uint32_t k_group = p.k_box5 ? C::kHalves * 1024 : 1024;
+    const uint32_t k_panel = p.k_box5 ? 1024 : C::kKPanel;
+    const uint64_t dK0 = ptx::sdesc_sw128(sK(0), 16, k_group);
     bool ok = wait_on(c, c.b(BQT), 0);
     for (int t = 0; ok && t < ntiles; ++t) {
       const int s = t % C::kKStages;
@@ -499,11 +514,9 @@ __device__ __forceinline__ void prefill_item(const Ctx& c, const WorkItem& it, c
         const uint32_t ts = tS + (t & 1) * kKvTile;
         // A = Q from TMEM (loaded once per item), B = the K tile from shared memory
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          constexpr int kPanel = C::kKPanel;
-          ptx::mma_ts(ts, tQ + kk * 8, dk + (((kk >> 2) * kPanel + (kk & 3) * 32) >> 4), kIdQK,
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ts(ts, tQ + kk * 8, dk + (((kk >> 2) * k_panel + (kk & 3) * 32) >> 4), kIdQK,
                       kk > 0 ? 1u : 0u);
-        }
         ptx::mma_commit(c.b(BS0 + (t & 1)));
         ptx::mma_commit(c.b(BKE0 + s));
       }
@@ -1401,7 +1414,15 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   const bool gather = !contig && a.page_size == 1;
   const int box_tok = gather ? 1 : (!contig && a.page_size == 8) ? 8 : kPageSize;
   const bool panel_boxes = dr != D;
-  {
+  // 8-token boxes of K carry every panel when the rows are full width: half
+  // the K boxes of a tile (an 8-key group per panel fills one box exactly)
+  const bool k_box5 = box_tok == 8 && !panel_boxes && !gather && D > 64;
+  if (k_box5) {
+    cuuint64_t dims[5] = {64, ntok, (cuuint64_t)(D / 64), (cuuint64_t)a.num_kv_heads, npages};
+    cuuint64_t strides[4] = {(cuuint64_t)a.num_kv_heads * dr2, 128, dr2, page_stride};
+    cuuint32_t box[5] = {64, 8, (cuuint32_t)(D / 64), 1, 1};
+    if (!encode(&tk, a.k_cache, 5, dims, strides, box, "k_cache")) return -1;
+  } else {
     // one 64-column panel of one kv head of box_tok tokens: dims {d, head, token, page}
     cuuint64_t dims[4] = {(cuuint64_t)dr, (cuuint64_t)a.num_kv_heads, ntok, npages};
     cuuint64_t strides[3] = {dr2, (cuuint64_t)a.num_kv_heads * dr2, page_stride};
@@ -1459,6 +1480,7 @@ int launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
   kp.dec_stages = decode_stages<D>(HG);
   kp.scale_log2 = a.sm_scale * kLog2e;
   kp.test_stall = a.test_stall;
+  kp.k_box5 = k_box5 ? 1 : 0;
   cudaError_t e = cudaFuncSetAttribute(mixed_attn_fwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return static_cast<int>(e);
