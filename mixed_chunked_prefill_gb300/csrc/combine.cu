@@ -60,14 +60,36 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineEntry* __rest
   const int n = e.num_splits;
   const int64_t pr0 = static_cast<int64_t>(e.part_row) + row;  // part k: row pr0 + k * e.rows
 
-  float M = neg_inf();
-  for (int k = lane; k < n; k += 32) M = fmaxf(M, part_lse[pr0 + static_cast<int64_t>(k) * e.rows]);
-  M = warp_max(M);
-
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  float L = 0.f;
+  float L = 0.f, M = neg_inf();
+  if (V == 4 && n <= 8) {
+    // few parts (every split chunk tile, most decodes): the LSEs and every
+    // part's slice of O are loaded at once, one memory latency for the row
+    float4 ov[8];
+    const float lk = lane < n ? part_lse[pr0 + static_cast<int64_t>(lane) * e.rows] : neg_inf();
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < n)
+        ov[j] = __ldg(reinterpret_cast<const float4*>(
+            part_o + (pr0 + static_cast<int64_t>(j) * e.rows) * D + lane * V));
+    M = warp_max(lk);
+    const float w = (lk == neg_inf()) ? 0.f : ptx::ex2((lk - M) * kLog2e);
+    L = w;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < n) {
+        const float wj = __shfl_sync(0xffffffffu, w, j);
+        acc[0] += wj * ov[j].x;
+        acc[1] += wj * ov[j].y;
+        acc[2] += wj * ov[j].z;
+        acc[3] += wj * ov[j].w;
+      }
+    }
+  } else {
+  for (int k = lane; k < n; k += 32) M = fmaxf(M, part_lse[pr0 + static_cast<int64_t>(k) * e.rows]);
+  M = warp_max(M);
   for (int k0 = 0; k0 < n; k0 += 32) {
     const int k = k0 + lane;
     const float lk = k < n ? part_lse[pr0 + static_cast<int64_t>(k) * e.rows] : neg_inf();
@@ -93,6 +115,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineEntry* __rest
         for (int v = 0; v < V; ++v) acc[v] += wj * __ldg(src + v);
       }
     }
+  }
   }
   L = warp_sum(L);
   const float inv = L > 0.f ? 1.f / L : 0.f;
